@@ -1,0 +1,342 @@
+"""Seeded synthetic workloads for the decode path (inputs only).
+
+Each workload is one decode layer: a pre-filled paged cache, the step's new
+tokens with their slots, the query of every sequence, the block tables and the
+context lengths after the step, and -- for parallel sampling -- the
+copy-on-write block pairs.  Both the CUDA path and the CPU oracle take their
+inputs from here; this module holds none of the attention arithmetic.
+
+Values are drawn with numpy's PCG64 from a seed, in float32, and rounded to the
+I/O type (fp16 through numpy, bf16 through torch's CPU cast, both round to
+nearest even).  Every array of element data holds raw bits: uint16 for fp16 and
+bf16.  Prefill values are drawn per segment (one sequence, or one shared prompt)
+from their own sub-seed, so any one sequence can be rebuilt without the others.
+
+Workload shapes (the five decode layers of the benchmark):
+
+=========================  =========================================================
+tiny_f16                   fp16, 8 heads = 8 KV heads, head_dim 64, block 16, 4
+                           sequences of 5/17/33/64 tokens, pool 64 blocks
+opt13b_f16                 OPT-13B layer: fp16, 40 x 128 MHA, block 16, batch 32,
+                           log-normal lengths (median 500, sigma 0.5, clip
+                           [1, 2048]), pool sized for 15,700 tokens (grown if the
+                           draw needs more), values 0.5 N(0,1)
+llama2_70b_bf16_gqa        Llama-2-70B layer: bf16, 64 query / 8 KV heads x 128,
+                           block 16, batch 64, lengths U[1024, 4096]
+cow_parallel_sampling_f16  fp16, 32 x 128, block 16, 16 prompts x 6 samples,
+                           shared 504-token prompt (last block half full), tails
+                           U[1, 256]; the step copies the shared last block for
+                           five of the six samples, appends every tail, decodes
+                           all 96 sequences
+llama2_7b_fp8_long         Llama-2-7B layer: E4M3 cache with one fp32 scale per
+                           tensor (K, V), bf16 q / inputs, 32 x 128, block 32,
+                           batch 16, lengths U[8192, 32768], 512-token partitions
+=========================  =========================================================
+
+The sizes come from the pages: OPT-13B's 5,120-wide layer and the 12 GB /
+15,700-token cache budget (「KV 缓存与分页注意力」 §03), Llama-2-70B's 64 query
+heads over 8 KV heads (same page, §11), Llama-2-7B's 4,096 width
+(「KV Cache从原理到实战」 §2.2), the 16-token default block (first page, §06),
+parallel samples sharing prompt blocks with copy-on-write (first page, §08) and
+8-bit float caches (first page, §11).
+"""
+from dataclasses import dataclass, field
+import math
+
+import numpy as np
+
+from .block_manager import BlockManager, BlockPool
+
+F16, BF16, E4M3 = 0, 1, 2
+DTYPE_NAMES = {F16: "f16", BF16: "bf16", E4M3: "e4m3"}
+E4M3_MAX = 448.0
+
+
+def _rng(*key):
+    return np.random.Generator(np.random.PCG64(list(key)))
+
+
+def _to_bits(x32, code):
+    """Round float32 values to fp16 / bf16 (nearest even) and return the bits."""
+    if code == F16:
+        return x32.astype(np.float16).view(np.uint16)
+    if code == BF16:
+        import torch
+        t = torch.from_numpy(np.ascontiguousarray(x32)).to(torch.bfloat16)
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    raise ValueError("inputs are fp16 or bf16")
+
+
+def bits_to_float32(bits, code):
+    """Exact float32 value of fp16 / bf16 bits (for scale calibration only)."""
+    if code == F16:
+        return bits.view(np.float16).astype(np.float32)
+    if code == BF16:
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+    raise ValueError(code)
+
+
+@dataclass
+class Segment:
+    """A run of prefill tokens written with one draw of values."""
+    key: tuple
+    slots: np.ndarray          # int64 [n]
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    cache_dtype: int
+    io_dtype: int
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    value_sigma: float
+    scale: float                       # softmax scale, an fp32 value
+    partition_size: int                # 0 = library default
+    context_lens: np.ndarray           # int32 [S], after the step
+    block_tables: np.ndarray           # int32 [S, max_blocks]
+    q: np.ndarray                      # uint16 [S, H, D]
+    segments: list                     # prefill segments
+    step_slots: np.ndarray             # int64 [T]
+    step_key: tuple
+    copy_pairs: np.ndarray             # int64 [n, 2]
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+    notes: dict = field(default_factory=dict)
+
+    # ------------------------------------------------------------ values
+    def values(self, key, n):
+        """(k, v) bits [n, Hkv, D] of the segment / step with this key."""
+        shape = (n, self.num_kv_heads, self.head_dim)
+        r = _rng(self.seed, *key)
+        k = r.standard_normal(shape, dtype=np.float32) * np.float32(self.value_sigma)
+        v = r.standard_normal(shape, dtype=np.float32) * np.float32(self.value_sigma)
+        return _to_bits(k, self.io_dtype), _to_bits(v, self.io_dtype)
+
+    def step_values(self):
+        return self.values(self.step_key, len(self.step_slots))
+
+    def prefill(self):
+        """Iterate (slots, k_bits, v_bits) over the prefill segments."""
+        for seg in self.segments:
+            k, v = self.values(seg.key, len(seg.slots))
+            yield seg.slots, k, v
+
+    # ------------------------------------------------------------ sizes
+    @property
+    def max_blocks_per_seq(self):
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self):
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    @property
+    def cache_elem_bytes(self):
+        return 1 if self.cache_dtype == E4M3 else 2
+
+    @property
+    def io_elem_bytes(self):
+        return 2
+
+    def decode_bytes(self):
+        """Algorithmic bytes of one decode call: every cached K/V element read
+        once per KV head, q and out once, the used block-table entries and the
+        context lengths."""
+        ctx = self.context_lens.astype(np.int64)
+        kv = int(ctx.sum()) * self.num_kv_heads * self.head_dim * 2 * self.cache_elem_bytes
+        qo = 2 * self.num_seqs * self.num_heads * self.head_dim * self.io_elem_bytes
+        bt = 4 * int(((ctx + self.block_size - 1) // self.block_size).sum())
+        return kv + qo + bt + 4 * self.num_seqs
+
+    def unique_kv_bytes(self):
+        """K/V bytes of the distinct physical blocks the decode touches,
+        counted at the tokens they hold (shared prompt blocks once)."""
+        seen = {}
+        for s in range(self.num_seqs):
+            ctx = int(self.context_lens[s])
+            nblk = (ctx + self.block_size - 1) // self.block_size
+            for i in range(nblk):
+                fill = min(self.block_size, ctx - i * self.block_size)
+                b = int(self.block_tables[s, i])
+                seen[b] = max(seen.get(b, 0), fill)
+        tokens = sum(seen.values())
+        return tokens * self.num_kv_heads * self.head_dim * 2 * self.cache_elem_bytes
+
+    def append_bytes(self):
+        t = int((self.step_slots >= 0).sum())
+        per = self.num_kv_heads * self.head_dim * 2 * (self.io_elem_bytes + self.cache_elem_bytes)
+        return t * (per + 8)
+
+    def copy_bytes(self):
+        blk = self.num_kv_heads * self.block_size * self.head_dim * self.cache_elem_bytes
+        return int(self.copy_pairs.shape[0]) * 2 * 2 * blk
+
+    # ------------------------------------------------------------ scales
+    def calibrate_fp8_scales(self):
+        """One scale per tensor: amax of every value written / 448 (fp32)."""
+        if self.cache_dtype != E4M3:
+            return
+        amax_k = np.float32(0.0)
+        amax_v = np.float32(0.0)
+        batches = list(self.prefill())
+        batches.append((self.step_slots,) + tuple(self.step_values()))
+        for _, k, v in batches:
+            amax_k = max(amax_k, np.abs(bits_to_float32(k, self.io_dtype)).max(initial=0))
+            amax_v = max(amax_v, np.abs(bits_to_float32(v, self.io_dtype)).max(initial=0))
+        self.k_scale = float(np.float32(amax_k) / np.float32(E4M3_MAX)) if amax_k > 0 else 1.0
+        self.v_scale = float(np.float32(amax_v) / np.float32(E4M3_MAX)) if amax_v > 0 else 1.0
+
+
+# ---------------------------------------------------------------- builders
+
+def _pool_and_manager(num_blocks, block_size, seed):
+    order = _rng(seed, 9).permutation(num_blocks)
+    pool = BlockPool(num_blocks, block_size, order=order)
+    return pool, BlockManager(pool)
+
+
+def _independent(name, seed, cache_dtype, io_dtype, num_heads, num_kv_heads, head_dim,
+                 block_size, ctx, value_sigma, num_blocks=None, pool_factor=1.25,
+                 min_blocks=0, partition_size=0, max_seg_tokens=4096):
+    """Sequences with independent contexts: prefill ctx-1 tokens, the step
+    appends each sequence's last token, decode over ctx tokens."""
+    ctx = np.asarray(ctx, dtype=np.int64)
+    need = int(((ctx + block_size - 1) // block_size).sum())
+    if num_blocks is None:
+        num_blocks = max(min_blocks, int(math.ceil(pool_factor * need)))
+    pool, mgr = _pool_and_manager(num_blocks, block_size, seed)
+    seqs = [mgr.new_sequence() for _ in ctx]
+    segments = []
+    for i, (s, n) in enumerate(zip(seqs, ctx)):
+        slots, pairs = mgr.append_tokens(s, int(n) - 1)
+        assert not pairs
+        for j in range(0, len(slots), max_seg_tokens):
+            segments.append(Segment(key=(1, i, j // max_seg_tokens),
+                                    slots=slots[j:j + max_seg_tokens]))
+    step = np.empty(len(seqs), dtype=np.int64)
+    for i, s in enumerate(seqs):
+        step[i], pair = mgr.append_slot(s)
+        assert pair is None
+    tables = BlockManager.block_table_array(seqs)
+    q = _to_bits(_rng(seed, 3).standard_normal((len(seqs), num_heads, head_dim),
+                                                 dtype=np.float32) * np.float32(value_sigma),
+                 io_dtype)
+    w = Workload(name=name, seed=seed, cache_dtype=cache_dtype, io_dtype=io_dtype,
+                 num_seqs=len(seqs), num_heads=num_heads, num_kv_heads=num_kv_heads,
+                 head_dim=head_dim, block_size=block_size, num_blocks=num_blocks,
+                 value_sigma=value_sigma,
+                 scale=float(np.float32(1.0) / np.float32(math.sqrt(head_dim))),
+                 partition_size=partition_size,
+                 context_lens=ctx.astype(np.int32), block_tables=tables, q=q,
+                 segments=segments, step_slots=step, step_key=(2,),
+                 copy_pairs=np.zeros((0, 2), dtype=np.int64))
+    w.notes["blocks_needed"] = need
+    w.notes["pool_blocks"] = num_blocks
+    w.notes["refcount_max"] = int(pool.refcount.max()) if num_blocks else 0
+    return w
+
+
+def tiny_f16(seed=1, ctx=(5, 17, 33, 64)):
+    return _independent("tiny_f16", seed, F16, F16, 8, 8, 64, 16, ctx, 1.0,
+                        num_blocks=64)
+
+
+def opt13b_f16(seed=2, num_seqs=32, median=500.0, sigma=0.5, max_len=2048):
+    z = _rng(seed, 0).standard_normal(num_seqs)
+    ctx = np.clip(np.rint(np.exp(math.log(median) + sigma * z)), 1, max_len).astype(np.int64)
+    # a 12 GB / 819,200-byte budget holds 15,700 tokens = 982 blocks of 16;
+    # the pool grows to the draw's need when that is larger
+    w = _independent("opt13b_f16", seed, F16, F16, 40, 40, 128, 16, ctx, 0.5,
+                     pool_factor=1.0, min_blocks=int(math.ceil(15700 / 16)))
+    w.notes["pool_rule"] = ("15,700-token budget" if w.num_blocks == 982
+                            else "grown to the draw's block count")
+    return w
+
+
+def llama2_70b_bf16_gqa(seed=3, num_seqs=64, lo=1024, hi=4096):
+    ctx = _rng(seed, 0).integers(lo, hi, size=num_seqs, endpoint=True)
+    return _independent("llama2_70b_bf16_gqa", seed, BF16, BF16, 64, 8, 128, 16, ctx, 1.0)
+
+
+def llama2_7b_fp8_long(seed=5, num_seqs=16, lo=8192, hi=32768, calibrate=True):
+    ctx = _rng(seed, 0).integers(lo, hi, size=num_seqs, endpoint=True)
+    w = _independent("llama2_7b_fp8_long", seed, E4M3, BF16, 32, 32, 128, 32, ctx, 1.0,
+                     partition_size=512)
+    if calibrate:
+        w.calibrate_fp8_scales()
+    return w
+
+
+def cow_parallel_sampling_f16(seed=4, num_prompts=16, samples=6, prompt_len=504,
+                              tail_lo=1, tail_hi=256, num_heads=32, head_dim=128,
+                              block_size=16):
+    """Shared prompts with copy-on-write at the first divergent write.
+
+    Set-up: each prompt's tokens are written once; ``samples`` sequences share
+    its blocks (reference count ``samples``).  The step: every sample appends
+    its tail; the first tail token of each of the first ``samples - 1`` samples
+    finds the half-full last prompt block shared and gets a private copy (the
+    (src, dst) pairs), the last sample writes in place.  ``copy_blocks`` runs
+    before the append, the decode reads all sequences."""
+    tails = _rng(seed, 0).integers(tail_lo, tail_hi, size=(num_prompts, samples),
+                                   endpoint=True)
+
+    def simulate(num_blocks, order_seed):
+        if order_seed is None:
+            pool = BlockPool(num_blocks, block_size)
+            mgr = BlockManager(pool)
+        else:
+            pool, mgr = _pool_and_manager(num_blocks, block_size, order_seed)
+        segs, seqs, step, pairs = [], [], [], []
+        for p in range(num_prompts):
+            root = mgr.new_sequence()
+            slots, pp = mgr.append_tokens(root, prompt_len)
+            assert not pp
+            segs.append(Segment(key=(1, p, 0), slots=slots))
+            group = [root] + [mgr.fork(root) for _ in range(samples - 1)]
+            seqs.extend(group)
+        refmax = int(pool.refcount.max())
+        for i, s in enumerate(seqs):
+            slots, pp = mgr.append_tokens(s, int(tails.reshape(-1)[i]))
+            step.append(slots)
+            pairs.extend(pp)
+        used = num_blocks - pool.num_free
+        return segs, seqs, np.concatenate(step), pairs, used, refmax, pool
+
+    _, _, _, _, used, _, _ = simulate(10 ** 7, None)
+    num_blocks = int(math.ceil(1.25 * used))
+    segs, seqs, step, pairs, used, refmax, pool = simulate(num_blocks, seed)
+    ctx = np.array([s.num_tokens for s in seqs], dtype=np.int64)
+    tables = BlockManager.block_table_array(seqs)
+    q = _to_bits(_rng(seed, 3).standard_normal((len(seqs), num_heads, head_dim),
+                                                 dtype=np.float32), F16)
+    w = Workload(name="cow_parallel_sampling_f16", seed=seed, cache_dtype=F16, io_dtype=F16,
+                 num_seqs=len(seqs), num_heads=num_heads, num_kv_heads=num_heads,
+                 head_dim=head_dim, block_size=block_size, num_blocks=num_blocks,
+                 value_sigma=1.0,
+                 scale=float(np.float32(1.0) / np.float32(math.sqrt(head_dim))),
+                 partition_size=0, context_lens=ctx.astype(np.int32), block_tables=tables,
+                 q=q, segments=segs, step_slots=step, step_key=(2,),
+                 copy_pairs=np.array(pairs, dtype=np.int64).reshape(-1, 2))
+    w.notes.update(blocks_used=used, pool_blocks=num_blocks, refcount_after_fork=refmax,
+                   refcount_after_step=pool.refcount.copy(), tails=tails)
+    return w
+
+
+WORKLOADS = {
+    "tiny_f16": tiny_f16,
+    "opt13b_f16": opt13b_f16,
+    "llama2_70b_bf16_gqa": llama2_70b_bf16_gqa,
+    "cow_parallel_sampling_f16": cow_parallel_sampling_f16,
+    "llama2_7b_fp8_long": llama2_7b_fp8_long,
+}
+
+
+def make(name, **kw):
+    return WORKLOADS[name](**kw)
