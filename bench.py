@@ -1,0 +1,469 @@
+"""Benchmark of the paged decode step on GB300.
+
+One step = the whole hot path over one batch: the copy-on-write block copies
+(when the workload has any), the append of the step's new tokens, and decode
+attention over every sequence (partition kernel + log-sum-exp reduce).  The
+cache is pre-filled once (untimed).  Between timed steps L2 is flushed by a
+512 MiB device write; the decode inputs are also larger than L2.
+
+Output: one JSON line on rank 0.  ``value`` is decode KV-read GB/s: algorithmic
+bytes of one decode (every cached K/V element once per KV head, q, out, the used
+block-table entries and the context lengths) over the decode time measured with
+CUDA events on the launch stream, summed over all ranks' work and divided by the
+slowest rank's time (replicas: every rank decodes its own batch).
+
+``--impl reference`` times the CPU oracle on the host cores on a bounded sample
+of the same workload instead (rank 0 only).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention KV-read GB/s (fraction of HBM peak); decode tokens/s"
+DEFAULT_WORKLOAD = "opt13b_f16"
+MODEL_LAYERS = {"opt13b_f16": 40, "llama2_70b_bf16_gqa": 80, "llama2_7b_fp8_long": 32,
+                "cow_parallel_sampling_f16": 40, "tiny_f16": 1}
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes per launch of the decode partition kernel from an ncu capture,
+# valid while csrc/decode.cu has the hash below (else reported as null)
+NCU_TRAFFIC = {}
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(values_by_rank_time, units):
+    """value = units summed over ranks / slowest rank's time."""
+    t = max(values_by_rank_time)
+    return sum(units) / t if t > 0 else 0.0
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed loop runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_decode_sample(w, state, seqs, reps):
+    """Time the oracle's decode on `seqs` of the workload, `reps` times."""
+    import oracle
+    q, bt, cl = w.q[seqs], w.block_tables[seqs], w.context_lens[seqs]
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.paged_attention_decode(state.k_cache, state.v_cache, w.cache_dtype, q, w.io_dtype,
+                                      bt, cl, w.scale, w.k_scale, w.v_scale)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(w, seqs):
+    ctx = w.context_lens[seqs].astype(np.int64)
+    kv = int(ctx.sum()) * w.num_kv_heads * w.head_dim * 2 * w.cache_elem_bytes
+    qo = 2 * len(seqs) * w.num_heads * w.head_dim * 2
+    bt = 4 * int(((ctx + w.block_size - 1) // w.block_size).sum())
+    return kv + qo + bt + 4 * len(seqs)
+
+
+class HostState:
+    """Host caches written through the oracle (the CPU arm's inputs)."""
+
+    def __init__(self, w, prefill):
+        import oracle
+        shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+        dt = np.uint8 if w.cache_elem_bytes == 1 else np.uint16
+        self.k_cache = np.zeros(shape, dt)
+        self.v_cache = np.zeros(shape, dt)
+        for slots, k, v in prefill:
+            oracle.kv_append(self.k_cache, self.v_cache, w.cache_dtype, k, v, w.io_dtype, slots,
+                             w.k_scale, w.v_scale)
+        if len(w.copy_pairs):
+            oracle.copy_blocks([self.k_cache], [self.v_cache], w.copy_pairs)
+        k, v = w.step_values()
+        oracle.kv_append(self.k_cache, self.v_cache, w.cache_dtype, k, v, w.io_dtype,
+                         w.step_slots, w.k_scale, w.v_scale)
+
+
+def pick_sample(w, budget_s, host_state):
+    """Sequences and repetitions for a bounded oracle run (~budget_s seconds)."""
+    seqs = np.arange(w.num_seqs)
+    one = oracle_decode_sample(w, host_state, seqs[:1], 1)
+    per_seq = max(one, 1e-4)
+    n = int(min(w.num_seqs, max(1, budget_s / per_seq)))
+    seqs = seqs[:n]
+    reps = 1
+    t = oracle_decode_sample(w, host_state, seqs, 1)
+    if t < budget_s / 4:
+        reps = int(max(1, min(20, budget_s / max(t, 1e-4))))
+    return seqs, reps
+
+
+def run_reference(args, w, prefill):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    hs = HostState(w, prefill)
+    cores = os.cpu_count() or 1
+    seqs, _ = pick_sample(w, 20.0 / max(1, args.steps + args.warmup), hs)
+    for _ in range(args.warmup):
+        oracle_decode_sample(w, hs, seqs, 1)
+    t = oracle_decode_sample(w, hs, seqs, args.steps)
+    per = t / max(1, args.steps)
+    gbs = sample_bytes(w, seqs) / per / 1e9
+    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "decode of %d of %d sequences per step (%d context "
+                                       "tokens)" % (len(seqs), w.num_seqs,
+                                                    int(w.context_lens[seqs].sum()))},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    return line
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def workload_config(w):
+    return {"workload": w.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "cache_dtype": {0: "f16", 1: "bf16", 2: "e4m3"}[w.cache_dtype],
+            "q_dtype": {0: "f16", 1: "bf16"}[w.io_dtype],
+            "context_tokens": int(w.context_lens.sum()),
+            "max_context_len": w.max_context_len,
+            "copy_pairs": int(len(w.copy_pairs)),
+            "step_tokens": int(len(w.step_slots)),
+            "l2": "flushed between steps by a 512 MiB write; decode inputs exceed the 129 MB L2",
+            "parallelism": "replicas"}
+
+
+def run_gpu(args, w, prefill):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+
+    from paged_kv_cache_130_gb300 import binding as B
+    from paged_kv_cache_130_gb300 import build as pkv_build
+    pkv_build.build()
+    B.load()
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+
+    shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    cdt = {0: torch.float16, 1: torch.bfloat16, 2: torch.uint8}[w.cache_dtype]
+    iodt = {0: torch.float16, 1: torch.bfloat16}[w.io_dtype]
+    k_cache = torch.zeros(shape, dtype=cdt, device=dev)
+    v_cache = torch.zeros(shape, dtype=cdt, device=dev)
+    desc = B.cache_desc(k_cache, v_cache, w.k_scale, w.v_scale)
+
+    def dev16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(iodt).to(dev)
+
+    for slots, k, v in prefill:
+        B.pkv_kv_append(desc, dev16(k), dev16(v), torch.from_numpy(slots).to(dev))
+    q = dev16(w.q)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    sk, sv = w.step_values()
+    step_k, step_v = dev16(sk), dev16(sv)
+    step_slots = torch.from_numpy(w.step_slots).to(dev)
+    pairs = torch.from_numpy(w.copy_pairs).to(dev) if len(w.copy_pairs) else None
+    ps = B.pkv_decode_partition_size(desc, w.partition_size)
+    ws_bytes = B.pkv_decode_workspace_bytes(desc, w.num_seqs, w.num_heads, w.max_context_len, ps)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    maxp = -(-w.max_context_len // ps)
+    launches_per_step = 1 + (1 if pairs is not None else 0) + 1 + (1 if maxp > 1 else 0)
+
+    def step(ev=None):
+        if pairs is not None:
+            B.pkv_copy_blocks(desc, pairs)
+        B.pkv_kv_append(desc, step_k, step_v, step_slots)
+        if ev is not None:
+            ev.record()
+        B.pkv_paged_attention_decode(desc, q, bt, cl, w.max_context_len, w.scale,
+                                     partition_size=ps, workspace=workspace, out=out)
+
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    evs = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step(e1)
+        e2.record()
+        evs.append((e0, e1, e2))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    step_ms = [a.elapsed_time(c) for a, _, c in evs]
+    dec_ms = [b.elapsed_time(c) for _, b, c in evs]
+    pre_ms = [a.elapsed_time(b) for a, b, _ in evs]
+
+    # the dominant kernel alone (partition kernel), for the roofline
+    part_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        B.pkv_paged_attention_partitions(desc, q, bt, cl, w.max_context_len, w.scale,
+                                         partition_size=ps, workspace=workspace, out=out)
+        b.record()
+        part_ms.append((a, b))
+    torch.cuda.synchronize()
+    part_ms = [a.elapsed_time(b) for a, b in part_ms]
+    clk = clocks.stop() if clocks else None
+
+    dec_s = sum(dec_ms) / 1e3
+    step_s = sum(step_ms) / 1e3
+    dbytes = w.decode_bytes()
+    if world > 1:
+        t = torch.tensor([dec_s, step_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dec_s, step_s = float(t[0]), float(t[1])
+    units = dbytes * args.steps * world
+    value = units / dec_s / 1e9
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_q = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(iodt).pin_memory()
+        h_k = torch.from_numpy(np.ascontiguousarray(sk).view(np.int16)).view(iodt).pin_memory()
+        h_v = torch.from_numpy(np.ascontiguousarray(sv).view(np.int16)).view(iodt).pin_memory()
+        h_slots = torch.from_numpy(w.step_slots).pin_memory()
+        h_bt = torch.from_numpy(w.block_tables).pin_memory()
+        h_cl = torch.from_numpy(w.context_lens).pin_memory()
+        h_pairs = torch.from_numpy(w.copy_pairs).pin_memory() if pairs is not None else None
+        h_out = torch.empty(out.shape, dtype=iodt).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
+        if h_pairs is not None:
+            h2d += h_pairs.numel() * 8
+        d2h = h_out.numel() * h_out.element_size()
+        e2e_ms = []
+        for i in range(args.steps + args.warmup):
+            flush.fill_(i & 0xff)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            q.copy_(h_q, non_blocking=True)
+            step_k.copy_(h_k, non_blocking=True)
+            step_v.copy_(h_v, non_blocking=True)
+            step_slots.copy_(h_slots, non_blocking=True)
+            bt.copy_(h_bt, non_blocking=True)
+            cl.copy_(h_cl, non_blocking=True)
+            if h_pairs is not None:
+                pairs.copy_(h_pairs, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            b.record()
+            b.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(a.elapsed_time(b))
+        e2e_s = sum(e2e_ms) / 1e3
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t[0])
+        e2e = {"value": dbytes * args.steps * world / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_s * 1e3 / args.steps}
+
+    peak, peak_kind = hbm_peak()
+    part_mean = sum(part_ms) / len(part_ms) / 1e3
+    achieved = dbytes / part_mean / 1e9
+    sha = _sha(os.path.join(ROOT, "paged_kv_cache_130_gb300", "csrc", "decode.cu"))
+    tr = NCU_TRAFFIC.get(w.name)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("decode_cu_sha") == sha else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "decode partition kernel (pkv_paged_attention_partitions)",
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(w),
+            "hbm_frac": value / peak,
+            "decode_ms": dec_s * 1e3 / args.steps,
+            "decode_tokens_per_s": w.num_seqs * world * args.steps / dec_s,
+            "model_tokens_per_s_attention_only":
+                w.num_seqs * world * args.steps / dec_s / MODEL_LAYERS.get(w.name, 1),
+            "step_ms": {"copy_and_append": statistics.mean(pre_ms),
+                        "decode": statistics.mean(dec_ms), "step": statistics.mean(step_ms)},
+            "decode_bytes": dbytes, "unique_kv_bytes": w.unique_kv_bytes(),
+            "roofline": roofline, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk, "wall_s": t_wall}
+    if w.unique_kv_bytes() != w.kv_bytes():
+        # shared prompt blocks: the same figure over distinct bytes only
+        ubytes = dbytes - w.kv_bytes() + w.unique_kv_bytes()
+        line["unique_bytes_gbs"] = ubytes * args.steps * world / dec_s / 1e9
+    if world > 1:
+        dist.barrier()
+    if rank == 0 and not args.no_cpu_baseline:
+        hs = HostState(w, prefill)
+        seqs, reps = pick_sample(w, 15.0, hs)
+        t = oracle_decode_sample(w, hs, seqs, reps)
+        line["cpu_baseline"] = {
+            "value": sample_bytes(w, seqs) * reps / t / 1e9, "unit": "GB/s",
+            "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": "oracle decode of %d of %d sequences x %d repetitions (%d context tokens "
+                      "each), fp64, all host threads" % (len(seqs), w.num_seqs, reps,
+                                                        int(w.context_lens[seqs].sum()))}
+    if world > 1 and dist.is_initialized():
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from paged_kv_cache_130_gb300 import workloads as W
+    world, rank, _ = dist_env()
+    if args.impl == "reference" and rank != 0:
+        return 0
+    w = W.make(args.workload)
+    prefill = list(w.prefill())
+    if args.impl == "reference":
+        line = run_reference(args, w, prefill)
+    else:
+        line = run_gpu(args, w, prefill)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

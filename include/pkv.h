@@ -1,0 +1,219 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache decode library (libpkv.so, sm_103a).
+ *
+ * The library implements the data-parallel hot path of PagedAttention: the
+ * per-token append of K/V into a cache of fixed-size physical blocks, the
+ * copy-on-write block copy, and single-query decode attention that walks each
+ * sequence's block table.  The operations are those of the pages
+ *   「KV 缓存与分页注意力」 (Laplace mini-world plate F55): §02 一次写一个词元
+ *   (each decode round computes and stores only the new token's K/V, then
+ *   attends over all earlier K/V), §06 像内存分页 (equal-size blocks, logical
+ *   vs physical), §07 块表 (block table; the kernel fetches K/V block by block
+ *   through it), §08 共用，写时复制 (shared blocks, copy before writing), §11
+ *   后来的做法 (query heads in groups sharing one K/V head; 8-bit float cache);
+ *   「Paged Attention in LLMs」 (Outcome School, Chinese translation), sections
+ *   "Paged Attention 如何工作" and "Block Table".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership.  The caller owns every buffer.  The library never allocates,
+ *   frees or synchronises; it keeps no state between calls and is thread-safe.
+ * Pointers.   "device" pointers must be CUDA device (or managed) memory of
+ *   the current device.  Element data (caches, q, k, v, out) must be 16-byte
+ *   aligned and dense row-major in the shapes given.
+ * Execution.  Every compute call is asynchronous on `stream` (NULL = the
+ *   legacy default stream).  Errors that the host can see (bad sizes, null or
+ *   misaligned pointers, unsupported shapes) return before anything is
+ *   launched.  A failed launch returns PKV_ERR_CUDA.
+ * Device-side checks.  Every index read from device memory (slot, block id,
+ *   context length, copy pair) is range-checked inside the kernels; an access
+ *   that would leave its buffer is skipped, never performed.  When `dev_err`
+ *   is non-NULL the kernel ORs the PKV_DEVERR_* bits of what it found into
+ *   that device int32 (the caller zeroes it and reads it back).
+ * Element types.  PKV_F16 (IEEE binary16), PKV_BF16, PKV_FP8_E4M3 (OCP E4M3,
+ *   the "fn" variant: no infinities, largest finite 448).
+ * Cache layout.  One layer's K cache and V cache are separate arrays of shape
+ *   [num_blocks][num_kv_heads][block_size][head_dim]; the slot of a token is
+ *   block * block_size + offset.  A (block, KV head) tile is therefore one
+ *   contiguous run of block_size * head_dim elements.
+ * Supported shapes.  head_dim in {64, 128}; block_size in {8, 16, 32};
+ *   num_heads a multiple of num_kv_heads.  A 16-bit cache is read with a q of
+ *   the same type; an FP8 cache with an fp16 or bf16 q.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same handle as cudaStream_t / CUstream). */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or count  */
+    PKV_ERR_UNSUPPORTED = 2,   /* shape or type combination not implemented   */
+    PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required  */
+    PKV_ERR_CUDA = 4           /* a kernel launch failed                      */
+} pkv_status;
+
+typedef enum pkv_dtype {
+    PKV_F16 = 0,
+    PKV_BF16 = 1,
+    PKV_FP8_E4M3 = 2
+} pkv_dtype;
+
+/* Bits a kernel ORs into *dev_err. */
+#define PKV_DEVERR_SLOT      1   /* slot >= num_blocks * block_size            */
+#define PKV_DEVERR_BLOCK_ID  2   /* block-table entry outside [0, num_blocks)  */
+#define PKV_DEVERR_CONTEXT   4   /* context length < 0, above max_context_len  */
+                                 /* or above max_blocks_per_seq * block_size   */
+#define PKV_DEVERR_COPY_PAIR 8   /* copy pair entry outside [0, num_blocks)    */
+
+/* One layer's cache.  k_cache / v_cache: device, caller-owned, layout above.
+ * k_scale / v_scale: for an FP8 cache, the stored code times the scale is the
+ * value (one fp32 scale per tensor); ignored (treated as 1) otherwise. */
+typedef struct pkv_cache_desc {
+    void* k_cache;
+    void* v_cache;
+    int64_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t head_dim;
+    int32_t cache_dtype;          /* pkv_dtype */
+    float k_scale;
+    float v_scale;
+} pkv_cache_desc;
+
+/* Human-readable name of a status code (static string). */
+const char* pkv_status_string(int32_t status);
+
+/* ---------------------------------------------------------------------------
+ * kv_append -- write each new token's K and V into its slot.
+ *   「KV 缓存与分页注意力」 §02 (the new token's K/V are computed once and kept)
+ *   and §07 (the slot comes from the sequence's block table).
+ *
+ * k, v          device [num_tokens][num_kv_heads][head_dim] of in_dtype
+ *               (PKV_F16 or PKV_BF16).
+ * slot_mapping  device int64 [num_tokens]; token t goes to block
+ *               slot / block_size, offset slot % block_size, every KV head.
+ *               A negative slot skips the token (padding).  A slot at or past
+ *               num_blocks * block_size is skipped and flagged.
+ * Result: with a cache of in_dtype the bytes are copied unchanged.  With an
+ *   FP8 cache each element is stored as E4M3(fp32(x) * (1.0f / scale)), round
+ *   to nearest even, saturating to +-448, scale = k_scale or v_scale.
+ *   Other type pairings return PKV_ERR_UNSUPPORTED.
+ * Precondition (not checked): the non-negative slots are distinct.
+ * num_tokens == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_kv_append(const pkv_cache_desc* cache,
+                         const void* k, const void* v, int32_t in_dtype,
+                         const int64_t* slot_mapping, int64_t num_tokens,
+                         int32_t* dev_err, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * copy_blocks -- copy-on-write block copy.
+ *   「KV 缓存与分页注意力」 §08 (before writing into a block that other
+ *   sequences share, the writer copies the block and writes into the copy).
+ *
+ * caches      host array of num_layers descriptors, all with the same
+ *             num_blocks / num_kv_heads / block_size / head_dim / cache_dtype.
+ * block_pairs device int64 [num_pairs][2] = (src, dst) physical block ids.
+ * Result: for every layer and pair, the whole dst block of K and of V (all
+ *   heads, all block_size slots) becomes a copy of the src block.  A pair with
+ *   an id outside [0, num_blocks) is skipped and flagged.
+ * Precondition (not checked): dst ids are distinct and no dst is also a src.
+ * num_pairs == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_copy_blocks(const pkv_cache_desc* caches, int32_t num_layers,
+                           const int64_t* block_pairs, int64_t num_pairs,
+                           int32_t* dev_err, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Decode attention -- one query token per sequence attends over its whole
+ * cached context, which the kernel reads block by block through the table.
+ *   「KV 缓存与分页注意力」 §02 and §07; grouped heads: §11.
+ *
+ * For sequence s and query head h, with kv head g = h / (num_heads /
+ * num_kv_heads) (consecutive query heads share a KV head) and c = context_lens[s]:
+ *   k_t = K[block_tables[s][t / bs]][g][t % bs][:] * k_scale,  t in [0, c)
+ *   v_t = V[...same...] * v_scale
+ *   x_t = scale * dot(q[s][h], k_t)
+ *   out[s][h][:] = sum_t exp(x_t - max x) v_t / sum_t exp(x_t - max x)
+ * computed with fp32 accumulation and rounded once (to nearest even) to
+ * q_dtype.  A context of length 0 gives out = 0.
+ *
+ * q             device [num_seqs][num_heads][head_dim] of q_dtype (F16/BF16).
+ * block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *               ceil(c / block_size) are never read.
+ * context_lens  device int32 [num_seqs].
+ * max_context_len  host upper bound of context_lens (sizes the grid and the
+ *               workspace); a longer context is flagged and its output zeroed.
+ * partition_size   tokens per split-context partition, a multiple of
+ *               block_size, or 0 for the library's choice
+ *               (pkv_decode_partition_size).  Contexts longer than one
+ *               partition are processed as independent partitions whose
+ *               partial results a log-sum-exp reduce merges.
+ * workspace     device scratch of at least pkv_decode_workspace_bytes(...)
+ *               bytes, 256-byte aligned; may be NULL when that size is 0.
+ * out           device [num_seqs][num_heads][head_dim] of q_dtype.
+ * Launches: one partition kernel, then (when max_context_len exceeds one
+ *   partition) the reduce kernel, chained with programmatic dependent launch.
+ * ------------------------------------------------------------------------- */
+int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t requested);
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
+                                  int32_t num_heads, int32_t max_context_len,
+                                  int32_t partition_size);
+
+pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache,
+                                      const void* q, int32_t q_dtype,
+                                      int32_t num_seqs, int32_t num_heads,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t max_context_len,
+                                      float scale, int32_t partition_size,
+                                      void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_err, void* out, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The two stages of pkv_paged_attention_decode, for callers (and timers) that
+ * schedule them separately.  Arguments mean the same as above.
+ *
+ * Workspace layout (fp32, P = ceil(max_context_len / partition_size)):
+ *   m[num_seqs][num_heads][P]   at byte 0
+ *   l[num_seqs][num_heads][P]   at byte round_up(4*S*H*P, 256)
+ *   o[num_seqs][num_heads][P][head_dim] at byte 2*round_up(4*S*H*P, 256)
+ * For partition p (tokens [p*partition_size, (p+1)*partition_size) of c):
+ *   m = max_t x_t * log2(e),  l = sum_t 2^(x_t*log2(e) - m),
+ *   o = sum_t 2^(x_t*log2(e) - m) * v_t.
+ * pkv_paged_attention_partitions writes these for every (s, h, p) of a
+ * context longer than one partition, and writes out[s][h] directly for a
+ * context of at most one partition.  pkv_lse_reduce merges, for every (s, h)
+ * whose context spans two or more partitions,
+ *   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p,
+ * and leaves the other rows of out untouched.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_attention_partitions(const pkv_cache_desc* cache,
+                                          const void* q, int32_t q_dtype,
+                                          int32_t num_seqs, int32_t num_heads,
+                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t max_context_len,
+                                          float scale, int32_t partition_size,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t* dev_err, void* out, pkv_stream_t stream);
+
+pkv_status pkv_lse_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                          const int32_t* context_lens, int32_t max_context_len,
+                          int32_t partition_size, const void* workspace,
+                          size_t workspace_bytes, int32_t out_dtype, void* out,
+                          pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

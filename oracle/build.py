@@ -5,6 +5,7 @@ Test infrastructure: building the checker is not using it.  The compile uses
 E4M3 encoding path relies on one plain fp32 multiply).
 """
 import os
+import platform
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -16,7 +17,9 @@ LIB = os.path.join(OUT_DIR, "libpkv_oracle.so")
 def build(force: bool = False) -> str:
     """Build the oracle library if it is missing or older than its source."""
     os.makedirs(OUT_DIR, exist_ok=True)
-    if (not force and os.path.exists(LIB)
+    stamp = LIB + ".arch"
+    if (not force and os.path.exists(LIB) and os.path.exists(stamp)
+            and open(stamp).read() == platform.machine()
             and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
         return LIB
     tmp = LIB + ".tmp.%d" % os.getpid()
@@ -25,6 +28,8 @@ def build(force: bool = False) -> str:
            "-o", tmp, SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(platform.machine())
     return LIB
 
 

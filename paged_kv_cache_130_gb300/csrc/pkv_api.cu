@@ -1,0 +1,378 @@
+// pkv_api.cu -- the C ABI of include/pkv.h: argument checks, launch choice.
+//
+// Every entry point validates what the host can see (pointers, alignment,
+// sizes, supported shapes) and returns before launching anything when a check
+// fails.  Nothing here allocates, frees or synchronises.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool is16(int32_t dt) { return dt == PKV_F16 || dt == PKV_BF16; }
+
+pkv_status check_cache(const pkv_cache_desc* c)
+{
+    if (c == nullptr || c->k_cache == nullptr || c->v_cache == nullptr)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(c->k_cache) || !aligned16(c->v_cache))
+        return PKV_ERR_INVALID_ARG;
+    if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->block_size <= 0 || c->head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (c->cache_dtype != PKV_F16 && c->cache_dtype != PKV_BF16 && c->cache_dtype != PKV_FP8_E4M3)
+        return PKV_ERR_INVALID_ARG;
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return PKV_ERR_UNSUPPORTED;
+    if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32)
+        return PKV_ERR_UNSUPPORTED;
+    if (c->cache_dtype == PKV_FP8_E4M3) {
+        if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f) || c->k_scale != c->k_scale ||
+            c->v_scale != c->v_scale)
+            return PKV_ERR_INVALID_ARG;
+    }
+    return PKV_OK;
+}
+
+pkv_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return PKV_OK;
+    if (e == cudaErrorNotSupported)
+        return PKV_ERR_UNSUPPORTED;
+    return PKV_ERR_CUDA;
+}
+
+struct WorkspaceLayout {
+    int64_t parts;
+    int64_t m_off, l_off, o_off, bytes;
+};
+
+WorkspaceLayout layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                       int32_t max_context_len, int32_t partition_size)
+{
+    WorkspaceLayout w{};
+    w.parts = partition_size > 0 ? ((int64_t)max_context_len + partition_size - 1) / partition_size
+                                 : 0;
+    if (w.parts <= 1) {
+        w.bytes = 0;
+        return w;
+    }
+    const int64_t rows = (int64_t)num_seqs * num_heads * w.parts;
+    const int64_t ml = round_up(4 * rows, 256);
+    w.m_off = 0;
+    w.l_off = ml;
+    w.o_off = 2 * ml;
+    w.bytes = 2 * ml + round_up(4 * rows * head_dim, 256);
+    return w;
+}
+
+int32_t resolve_partition(const pkv_cache_desc* c, int32_t requested)
+{
+    if (requested > 0)
+        return requested;
+    // about 128 KiB of K+V per partition of one KV head
+    const int32_t elem = c->cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
+    int32_t tokens = (int32_t)(131072 / (2 * c->head_dim * elem));
+    tokens = tokens / c->block_size * c->block_size;
+    return tokens < c->block_size ? c->block_size : tokens;
+}
+
+pkv_status decode_checks(const pkv_cache_desc* cache, const void* q, int32_t q_dtype,
+                         int32_t num_seqs, int32_t num_heads, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         int32_t max_context_len, int32_t partition_size, const void* out)
+{
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK)
+        return st;
+    if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq < 0 || max_context_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_heads % cache->num_kv_heads != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (!is16(q_dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (partition_size < 0 || (partition_size > 0 && partition_size % cache->block_size != 0))
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return PKV_OK;
+    if (q == nullptr || out == nullptr || context_lens == nullptr || !aligned16(q) ||
+        !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    if (max_context_len > 0 && (block_tables == nullptr || max_blocks_per_seq <= 0))
+        return PKV_ERR_INVALID_ARG;
+    if (!pkv::decode_shape_supported(cache->cache_dtype, q_dtype, cache->head_dim,
+                                     cache->block_size))
+        return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+pkv_status launch_partitions(const pkv_cache_desc* cache, const void* q, int32_t q_dtype,
+                             int32_t num_seqs, int32_t num_heads, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             int32_t max_context_len, float scale, int32_t partition,
+                             void* workspace, const WorkspaceLayout& wl, int32_t* dev_err,
+                             void* out, cudaStream_t stream)
+{
+    pkv::DecodeParams p{};
+    p.k_cache = cache->k_cache;
+    p.v_cache = cache->v_cache;
+    p.num_blocks = cache->num_blocks;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.block_size = cache->block_size;
+    p.head_dim = cache->head_dim;
+    p.cache_dtype = cache->cache_dtype;
+    const bool fp8 = cache->cache_dtype == PKV_FP8_E4M3;
+    p.k_scale = fp8 ? cache->k_scale : 1.f;
+    p.v_scale = fp8 ? cache->v_scale : 1.f;
+    p.q = q;
+    p.q_dtype = q_dtype;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.group = num_heads / cache->num_kv_heads;
+    p.block_tables = block_tables;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.max_context_len = max_context_len;
+    p.partition_size = partition;
+    p.max_partitions = wl.parts < 1 ? 1 : (int32_t)wl.parts;
+    p.qk_scale_log2 = scale * 1.4426950408889634f * p.k_scale;
+    char* ws = reinterpret_cast<char*>(workspace);
+    p.ws_m = wl.bytes ? reinterpret_cast<float*>(ws + wl.m_off) : nullptr;
+    p.ws_l = wl.bytes ? reinterpret_cast<float*>(ws + wl.l_off) : nullptr;
+    p.ws_o = wl.bytes ? reinterpret_cast<float*>(ws + wl.o_off) : nullptr;
+    p.dev_err = dev_err;
+    p.out = out;
+    return from_cuda(pkv::launch_decode_partitions(p, stream));
+}
+
+pkv_status launch_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                         const int32_t* context_lens, int32_t max_context_len, int32_t partition,
+                         const void* workspace, const WorkspaceLayout& wl, int32_t out_dtype,
+                         void* out, cudaStream_t stream, bool pdl)
+{
+    if (wl.bytes == 0)
+        return PKV_OK;
+    pkv::ReduceParams r{};
+    r.num_seqs = num_seqs;
+    r.num_heads = num_heads;
+    r.head_dim = head_dim;
+    r.context_lens = context_lens;
+    r.max_context_len = max_context_len;
+    r.partition_size = partition;
+    r.max_partitions = (int32_t)wl.parts;
+    const char* ws = reinterpret_cast<const char*>(workspace);
+    r.ws_m = reinterpret_cast<const float*>(ws + wl.m_off);
+    r.ws_l = reinterpret_cast<const float*>(ws + wl.l_off);
+    r.ws_o = reinterpret_cast<const float*>(ws + wl.o_off);
+    r.out_dtype = out_dtype;
+    r.out = out;
+    return from_cuda(pkv::launch_lse_reduce(r, stream, pdl));
+}
+
+pkv_status check_workspace(const WorkspaceLayout& wl, const void* workspace, size_t bytes)
+{
+    if (wl.bytes == 0)
+        return PKV_OK;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return PKV_ERR_WORKSPACE;
+    if ((int64_t)bytes < wl.bytes)
+        return PKV_ERR_WORKSPACE;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int32_t status)
+{
+    switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PKV_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+    }
+}
+
+pkv_status pkv_kv_append(const pkv_cache_desc* cache, const void* k, const void* v,
+                         int32_t in_dtype, const int64_t* slot_mapping, int64_t num_tokens,
+                         int32_t* dev_err, pkv_stream_t stream)
+{
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK)
+        return st;
+    if (num_tokens < 0 || !is16(in_dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return PKV_OK;
+    if (k == nullptr || v == nullptr || slot_mapping == nullptr || !aligned16(k) || !aligned16(v))
+        return PKV_ERR_INVALID_ARG;
+    if (cache->cache_dtype != in_dtype && cache->cache_dtype != PKV_FP8_E4M3)
+        return PKV_ERR_UNSUPPORTED;
+    pkv::AppendParams p{};
+    p.k_cache = cache->k_cache;
+    p.v_cache = cache->v_cache;
+    p.num_blocks = cache->num_blocks;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.block_size = cache->block_size;
+    p.head_dim = cache->head_dim;
+    p.cache_dtype = cache->cache_dtype;
+    p.k_inv_scale = cache->cache_dtype == PKV_FP8_E4M3 ? 1.0f / cache->k_scale : 1.f;
+    p.v_inv_scale = cache->cache_dtype == PKV_FP8_E4M3 ? 1.0f / cache->v_scale : 1.f;
+    p.k = k;
+    p.v = v;
+    p.in_dtype = in_dtype;
+    p.slot_mapping = slot_mapping;
+    p.num_tokens = num_tokens;
+    p.dev_err = dev_err;
+    return from_cuda(pkv::launch_kv_append(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_copy_blocks(const pkv_cache_desc* caches, int32_t num_layers,
+                           const int64_t* block_pairs, int64_t num_pairs, int32_t* dev_err,
+                           pkv_stream_t stream)
+{
+    if (caches == nullptr || num_layers <= 0 || num_pairs < 0)
+        return PKV_ERR_INVALID_ARG;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        pkv_status st = check_cache(&caches[l]);
+        if (st != PKV_OK)
+            return st;
+        const pkv_cache_desc& a = caches[0];
+        const pkv_cache_desc& b = caches[l];
+        if (a.num_blocks != b.num_blocks || a.num_kv_heads != b.num_kv_heads ||
+            a.block_size != b.block_size || a.head_dim != b.head_dim ||
+            a.cache_dtype != b.cache_dtype)
+            return PKV_ERR_INVALID_ARG;
+    }
+    if (num_pairs == 0)
+        return PKV_OK;
+    if (block_pairs == nullptr)
+        return PKV_ERR_INVALID_ARG;
+    const pkv_cache_desc& c0 = caches[0];
+    const int64_t elem = c0.cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
+    pkv::CopyParams p{};
+    p.num_blocks = c0.num_blocks;
+    p.block_bytes = (int64_t)c0.num_kv_heads * c0.block_size * c0.head_dim * elem;
+    p.dev_err = dev_err;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int32_t l0 = 0; l0 < num_layers; l0 += pkv::kCopyMaxLayers) {
+        const int32_t nl = num_layers - l0 < pkv::kCopyMaxLayers ? num_layers - l0
+                                                                 : pkv::kCopyMaxLayers;
+        p.num_layers = nl;
+        for (int32_t i = 0; i < nl; ++i) {
+            p.k[i] = caches[l0 + i].k_cache;
+            p.v[i] = caches[l0 + i].v_cache;
+        }
+        for (int64_t q0 = 0; q0 < num_pairs; q0 += 65535) {
+            p.pairs = block_pairs + 2 * q0;
+            p.num_pairs = num_pairs - q0 < 65535 ? num_pairs - q0 : 65535;
+            pkv_status st = from_cuda(pkv::launch_copy_blocks(p, s));
+            if (st != PKV_OK)
+                return st;
+        }
+    }
+    return PKV_OK;
+}
+
+int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t requested)
+{
+    if (cache == nullptr || cache->block_size <= 0 || cache->head_dim <= 0)
+        return 0;
+    return resolve_partition(cache, requested);
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
+                                  int32_t num_heads, int32_t max_context_len,
+                                  int32_t partition_size)
+{
+    if (cache == nullptr || cache->block_size <= 0 || cache->head_dim <= 0 || num_seqs <= 0 ||
+        num_heads <= 0 || max_context_len <= 0 || partition_size < 0)
+        return 0;
+    const int32_t part = resolve_partition(cache, partition_size);
+    return (size_t)layout(num_seqs, num_heads, cache->head_dim, max_context_len, part).bytes;
+}
+
+pkv_status pkv_paged_attention_partitions(const pkv_cache_desc* cache, const void* q,
+                                          int32_t q_dtype, int32_t num_seqs, int32_t num_heads,
+                                          const int32_t* block_tables,
+                                          int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t max_context_len,
+                                          float scale, int32_t partition_size, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_err, void* out,
+                                          pkv_stream_t stream)
+{
+    pkv_status st = decode_checks(cache, q, q_dtype, num_seqs, num_heads, block_tables,
+                                  max_blocks_per_seq, context_lens, max_context_len,
+                                  partition_size, out);
+    if (st != PKV_OK || num_seqs == 0)
+        return st;
+    const int32_t part = resolve_partition(cache, partition_size);
+    const WorkspaceLayout wl = layout(num_seqs, num_heads, cache->head_dim, max_context_len, part);
+    st = check_workspace(wl, workspace, workspace_bytes);
+    if (st != PKV_OK)
+        return st;
+    return launch_partitions(cache, q, q_dtype, num_seqs, num_heads, block_tables,
+                             max_blocks_per_seq, context_lens, max_context_len, scale, part,
+                             workspace, wl, dev_err, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_lse_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                          const int32_t* context_lens, int32_t max_context_len,
+                          int32_t partition_size, const void* workspace, size_t workspace_bytes,
+                          int32_t out_dtype, void* out, pkv_stream_t stream)
+{
+    if (num_seqs < 0 || num_heads <= 0 || max_context_len < 0 || partition_size <= 0 ||
+        (head_dim != 64 && head_dim != 128) || !is16(out_dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return PKV_OK;
+    if (context_lens == nullptr || out == nullptr || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    const WorkspaceLayout wl = layout(num_seqs, num_heads, head_dim, max_context_len,
+                                      partition_size);
+    pkv_status st = check_workspace(wl, workspace, workspace_bytes);
+    if (st != PKV_OK)
+        return st;
+    return launch_reduce(num_seqs, num_heads, head_dim, context_lens, max_context_len,
+                         partition_size, workspace, wl, out_dtype, out,
+                         reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, const void* q, int32_t q_dtype,
+                                      int32_t num_seqs, int32_t num_heads,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t max_context_len,
+                                      float scale, int32_t partition_size, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_err, void* out,
+                                      pkv_stream_t stream)
+{
+    pkv_status st = decode_checks(cache, q, q_dtype, num_seqs, num_heads, block_tables,
+                                  max_blocks_per_seq, context_lens, max_context_len,
+                                  partition_size, out);
+    if (st != PKV_OK || num_seqs == 0)
+        return st;
+    const int32_t part = resolve_partition(cache, partition_size);
+    const WorkspaceLayout wl = layout(num_seqs, num_heads, cache->head_dim, max_context_len, part);
+    st = check_workspace(wl, workspace, workspace_bytes);
+    if (st != PKV_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = launch_partitions(cache, q, q_dtype, num_seqs, num_heads, block_tables,
+                           max_blocks_per_seq, context_lens, max_context_len, scale, part,
+                           workspace, wl, dev_err, out, s);
+    if (st != PKV_OK)
+        return st;
+    return launch_reduce(num_seqs, num_heads, cache->head_dim, context_lens, max_context_len,
+                         part, workspace, wl, q_dtype, out, s, true);
+}
+
+}  // extern "C"

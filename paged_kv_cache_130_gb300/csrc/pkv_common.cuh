@@ -1,0 +1,148 @@
+// pkv_common.cuh -- element types, vector memory access and conversions shared
+// by the paged KV-cache kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kF16 = PKV_F16;
+constexpr int kBF16 = PKV_BF16;
+constexpr int kE4M3 = PKV_FP8_E4M3;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int DT>
+struct Elem {
+    static constexpr int bytes = (DT == kE4M3) ? 1 : 2;
+    static constexpr int per_vec = 16 / bytes;     // elements in one 16-byte vector
+};
+
+// ------------------------------------------------------------------ loads
+
+// 16-byte load of data that is read once (K/V tiles): skip L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 16-byte read-only load through the normal cached path.
+__device__ __forceinline__ uint4 ld_ro(const void* p)
+{
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v)
+{
+    *reinterpret_cast<uint4*>(p) = v;
+}
+
+// ------------------------------------------------------------------ conversions
+
+// Two packed 16-bit values (low half = element 0) to float.
+template <int DT>
+__device__ __forceinline__ float2 unpack2(uint32_t w);
+
+template <>
+__device__ __forceinline__ float2 unpack2<kF16>(uint32_t w)
+{
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    return __half22float2(h);
+}
+
+template <>
+__device__ __forceinline__ float2 unpack2<kBF16>(uint32_t w)
+{
+    // bfloat16 is the upper half of an fp32 value
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Two E4M3 codes (low byte = element 0) to float, through the hardware
+// e4m3x2 -> f16x2 conversion (exact: every E4M3 value is an fp16 value).
+__device__ __forceinline__ float2 unpack_e4m3x2(uint16_t w)
+{
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w), __NV_E4M3);
+    __half2 hh = *reinterpret_cast<__half2*>(&h);
+    return __half22float2(hh);
+}
+
+// 16 bytes of cache data -> EPV floats.
+template <int DT>
+__device__ __forceinline__ void unpack_vec(const uint4& v, float* out)
+{
+    if constexpr (DT == kE4M3) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 a = unpack_e4m3x2(static_cast<uint16_t>(w[i] & 0xffffu));
+            float2 b = unpack_e4m3x2(static_cast<uint16_t>(w[i] >> 16));
+            out[4 * i + 0] = a.x;
+            out[4 * i + 1] = a.y;
+            out[4 * i + 2] = b.x;
+            out[4 * i + 3] = b.y;
+        }
+    } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 a = unpack2<DT>(w[i]);
+            out[2 * i + 0] = a.x;
+            out[2 * i + 1] = a.y;
+        }
+    }
+}
+
+// fp32 -> 16-bit element bits, round to nearest even.
+template <int DT>
+__device__ __forceinline__ uint16_t round_to(float x)
+{
+    if constexpr (DT == kF16) {
+        return __half_as_ushort(__float2half_rn(x));
+    } else {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi)
+{
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Two floats -> two E4M3 codes (low byte = first), round to nearest even,
+// saturating to the largest finite value.
+__device__ __forceinline__ uint16_t e4m3x2_satfinite(float a, float b)
+{
+    return static_cast<uint16_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// ------------------------------------------------------------------ misc
+
+__device__ __forceinline__ void flag_error(int32_t* dev_err, int32_t bit)
+{
+    if (dev_err != nullptr)
+        atomicOr(dev_err, bit);
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue; wait until the previous kernel's memory is visible.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_primary()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace pkv

@@ -1,0 +1,94 @@
+// pkv_internal.h -- launch interface between the C ABI (pkv_api.cu) and the
+// kernel translation units.  Not installed; not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct DecodeParams {
+    const void* k_cache;
+    const void* v_cache;
+    int64_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t head_dim;
+    int32_t cache_dtype;
+    float k_scale;
+    float v_scale;
+    const void* q;
+    int32_t q_dtype;
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t group;                 // num_heads / num_kv_heads
+    const int32_t* block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t* context_lens;
+    int32_t max_context_len;
+    int32_t partition_size;
+    int32_t max_partitions;        // ceil(max_context_len / partition_size)
+    float qk_scale_log2;           // scale * log2(e) * k_scale
+    float* ws_m;
+    float* ws_l;
+    float* ws_o;
+    int32_t* dev_err;
+    void* out;
+};
+
+struct ReduceParams {
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t head_dim;
+    const int32_t* context_lens;
+    int32_t max_context_len;
+    int32_t partition_size;
+    int32_t max_partitions;
+    const float* ws_m;
+    const float* ws_l;
+    const float* ws_o;
+    int32_t out_dtype;
+    void* out;
+};
+
+struct AppendParams {
+    void* k_cache;
+    void* v_cache;
+    int64_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t head_dim;
+    int32_t cache_dtype;
+    float k_inv_scale;
+    float v_inv_scale;
+    const void* k;
+    const void* v;
+    int32_t in_dtype;
+    const int64_t* slot_mapping;
+    int64_t num_tokens;
+    int32_t* dev_err;
+};
+
+constexpr int kCopyMaxLayers = 64;
+
+struct CopyParams {
+    void* k[kCopyMaxLayers];
+    void* v[kCopyMaxLayers];
+    int32_t num_layers;
+    int64_t num_blocks;
+    int64_t block_bytes;
+    const int64_t* pairs;
+    int64_t num_pairs;
+    int32_t* dev_err;
+};
+
+// Each returns cudaSuccess, or cudaErrorNotSupported for a shape without a kernel.
+cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_lse_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
+
+// Which decode kernel a shape selects (for the host checks and tests).
+bool decode_shape_supported(int cache_dtype, int q_dtype, int head_dim, int block_size);
+
+}  // namespace pkv

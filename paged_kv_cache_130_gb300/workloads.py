@@ -144,6 +144,11 @@ class Workload:
     def io_elem_bytes(self):
         return 2
 
+    def kv_bytes(self):
+        """K/V bytes one decode reads: every cached element once per KV head."""
+        ctx = self.context_lens.astype(np.int64)
+        return int(ctx.sum()) * self.num_kv_heads * self.head_dim * 2 * self.cache_elem_bytes
+
     def decode_bytes(self):
         """Algorithmic bytes of one decode call: every cached K/V element read
         once per KV head, q and out once, the used block-table entries and the

@@ -1,0 +1,110 @@
+"""The C-ABI library builds, loads and exports every symbol include/pkv.h
+declares; host-side argument checks reject bad calls before any launch.
+
+These run without a GPU: every call below fails a host check (or is a pure
+host query), so nothing is launched and no pointer is dereferenced.
+"""
+import ctypes
+
+import pytest
+
+from paged_kv_cache_130_gb300 import binding as B
+from paged_kv_cache_130_gb300 import build as pkv_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return B.load()
+
+
+def _desc(**kw):
+    d = dict(k_cache=0x10000, v_cache=0x20000, num_blocks=64, num_kv_heads=8, block_size=16,
+             head_dim=128, cache_dtype=B.PKV_F16, k_scale=1.0, v_scale=1.0)
+    d.update(kw)
+    return B.CacheDesc(**d)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = B.header_functions()
+    assert {"pkv_kv_append", "pkv_copy_blocks", "pkv_paged_attention_decode",
+            "pkv_paged_attention_partitions", "pkv_lse_reduce", "pkv_decode_workspace_bytes",
+            "pkv_decode_partition_size", "pkv_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert B.pkv_status_string(0) == "ok"
+    assert "workspace" in B.pkv_status_string(B.PKV_ERR_WORKSPACE)
+    assert B.pkv_status_string(99) == "unknown status"
+
+
+def test_partition_size_and_workspace(lib):
+    d = _desc()
+    assert B.pkv_decode_partition_size(d, 0) == 256          # 128 KiB of fp16 K+V
+    assert B.pkv_decode_partition_size(d, 64) == 64
+    f8 = _desc(cache_dtype=B.PKV_FP8_E4M3, block_size=32)
+    assert B.pkv_decode_partition_size(f8, 0) == 512
+    # a context within one partition needs no workspace
+    assert B.pkv_decode_workspace_bytes(d, 4, 8, 256, 0) == 0
+    s, h, p, dim = 3, 8, 3, 128
+    ml = -(-4 * s * h * p // 256) * 256
+    want = 2 * ml + -(-4 * s * h * p * dim // 256) * 256
+    assert B.pkv_decode_workspace_bytes(d, s, h, 700, 0) == want
+
+
+def _append(lib, desc, k=0x1000, v=0x2000, in_dtype=B.PKV_F16, slots=0x3000, n=4):
+    return lib.pkv_kv_append(ctypes.byref(desc), ctypes.c_void_p(k), ctypes.c_void_p(v),
+                             in_dtype, ctypes.c_void_p(slots), n, None, None)
+
+
+def test_append_host_checks(lib):
+    assert _append(lib, _desc(head_dim=96)) == B.PKV_ERR_UNSUPPORTED
+    assert _append(lib, _desc(block_size=12)) == B.PKV_ERR_UNSUPPORTED
+    assert _append(lib, _desc(k_cache=0x10001)) == B.PKV_ERR_INVALID_ARG
+    assert _append(lib, _desc(), k=0x1004) == B.PKV_ERR_INVALID_ARG
+    assert _append(lib, _desc(), slots=0) == B.PKV_ERR_INVALID_ARG
+    assert _append(lib, _desc(), n=-1) == B.PKV_ERR_INVALID_ARG
+    assert _append(lib, _desc(), in_dtype=B.PKV_FP8_E4M3) == B.PKV_ERR_INVALID_ARG
+    assert _append(lib, _desc(cache_dtype=B.PKV_BF16)) == B.PKV_ERR_UNSUPPORTED
+    assert _append(lib, _desc(cache_dtype=B.PKV_FP8_E4M3, k_scale=0.0)) == B.PKV_ERR_INVALID_ARG
+    assert _append(lib, _desc(), n=0) == B.PKV_OK                 # no-op, nothing launched
+
+
+def _decode(lib, desc, q_dtype=B.PKV_F16, S=2, H=8, bt=0x4000, mb=4, ctx=0x5000, maxctx=64,
+            part=0, ws=None, ws_bytes=0, out=0x6000, q=0x7000, fn="pkv_paged_attention_decode"):
+    return getattr(lib, fn)(ctypes.byref(desc), ctypes.c_void_p(q), q_dtype, S, H,
+                            ctypes.c_void_p(bt), mb, ctypes.c_void_p(ctx), maxctx,
+                            ctypes.c_float(0.1), part, ctypes.c_void_p(ws), ws_bytes, None,
+                            ctypes.c_void_p(out), None)
+
+
+@pytest.mark.parametrize("fn", ["pkv_paged_attention_decode", "pkv_paged_attention_partitions"])
+def test_decode_host_checks(lib, fn):
+    d = _desc()
+    assert _decode(lib, d, H=12, fn=fn) == B.PKV_ERR_INVALID_ARG          # 12 % 8 != 0
+    assert _decode(lib, d, q_dtype=B.PKV_BF16, fn=fn) == B.PKV_ERR_UNSUPPORTED
+    assert _decode(lib, d, part=24, fn=fn) == B.PKV_ERR_INVALID_ARG       # not a multiple of 16
+    assert _decode(lib, d, out=0x6002, fn=fn) == B.PKV_ERR_INVALID_ARG
+    assert _decode(lib, d, ctx=0, fn=fn) == B.PKV_ERR_INVALID_ARG
+    assert _decode(lib, _desc(head_dim=80), fn=fn) == B.PKV_ERR_UNSUPPORTED
+    # three partitions need a workspace
+    assert _decode(lib, d, maxctx=700, fn=fn) == B.PKV_ERR_WORKSPACE
+    assert _decode(lib, d, maxctx=700, ws=0x100010, ws_bytes=1 << 20, fn=fn) == \
+        B.PKV_ERR_WORKSPACE                                              # misaligned
+    assert _decode(lib, d, maxctx=700, ws=0x100000, ws_bytes=16, fn=fn) == B.PKV_ERR_WORKSPACE
+    assert _decode(lib, d, S=0, fn=fn) == B.PKV_OK                       # nothing to do
+
+
+def test_copy_and_reduce_host_checks(lib):
+    arr = (B.CacheDesc * 2)(_desc(), _desc(num_blocks=65))
+    assert lib.pkv_copy_blocks(arr, 2, ctypes.c_void_p(0x1000), 3, None, None) == \
+        B.PKV_ERR_INVALID_ARG                                            # layers differ
+    arr = (B.CacheDesc * 1)(_desc())
+    assert lib.pkv_copy_blocks(arr, 1, None, 3, None, None) == B.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy_blocks(arr, 1, None, 0, None, None) == B.PKV_OK
+    assert lib.pkv_lse_reduce(2, 8, 96, ctypes.c_void_p(0x1000), 100, 32, None, 0, 0,
+                              ctypes.c_void_p(0x2000), None) == B.PKV_ERR_INVALID_ARG
+    assert lib.pkv_lse_reduce(2, 8, 128, ctypes.c_void_p(0x1000), 100, 32, None, 0, 0,
+                              ctypes.c_void_p(0x2000), None) == B.PKV_ERR_WORKSPACE
