@@ -77,6 +77,11 @@ def _contig(a, dtype):
     return a
 
 
+def _check_rows(bt, cl, num_seqs):
+    if bt.ndim != 2 or bt.shape[0] != num_seqs or cl.shape != (num_seqs,):
+        raise ValueError("block_tables / context_lens do not match the number of sequences")
+
+
 def _elem_np(code):
     return np.uint8 if code == E4M3 else np.uint16
 
@@ -118,6 +123,8 @@ def gather(cache, cache_dtype, table_row, context_len, kv_head, scale=1.0):
     cache = _contig(cache, _elem_np(cache_dtype))
     nb, hkv, bs, d = cache.shape
     row = _contig(np.asarray(table_row, dtype=np.int32), np.int32)
+    if row.ndim != 1 or row.size * bs < context_len:
+        raise ValueError("the table row holds fewer blocks than the context needs")
     out = np.empty((context_len, d), np.float64)
     rc = _load().pkvo_gather(_ptr(cache), cache_dtype, nb, hkv, bs, d, _ptr(row),
                              context_len, kv_head, float(scale), _ptr(out))
@@ -172,6 +179,7 @@ def paged_attention_decode(k_cache, v_cache, cache_dtype, q, q_dtype, block_tabl
     assert dq == d
     bt = _contig(np.asarray(block_tables, dtype=np.int32), np.int32)
     cl = _contig(np.asarray(context_lens, dtype=np.int32), np.int32)
+    _check_rows(bt, cl, s)
     out = np.zeros((s, h, d), np.float64)
     rc = _load().pkvo_paged_attention_decode(
         _ptr(k_cache), _ptr(v_cache), cache_dtype, nb, hkv, bs, d,
@@ -195,6 +203,7 @@ def attention_range(k_cache, v_cache, cache_dtype, q, q_dtype, block_tables, con
     s, h, _ = q.shape
     bt = _contig(np.asarray(block_tables, dtype=np.int32), np.int32)
     cl = _contig(np.asarray(context_lens, dtype=np.int32), np.int32)
+    _check_rows(bt, cl, s)
     o = np.zeros((s, h, d), np.float64)
     m = np.zeros((s, h), np.float64)
     l = np.zeros((s, h), np.float64)

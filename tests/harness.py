@@ -145,14 +145,29 @@ def out_to_double(out):
     return out.detach().float().cpu().numpy().astype(np.float64)
 
 
-def assert_attention_close(got, ref, what=""):
-    """|got - ref| <= 2e-3 + 2e-3 |ref| elementwise (got rounded to fp16/bf16)."""
+def half_ulp(ref, out_dtype):
+    """Half the spacing of the output format (fp16 / bf16) at |ref|: the most
+    that the one final round-to-nearest of the output can move a value."""
+    a = np.abs(np.asarray(ref, np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    if out_dtype == W.BF16:
+        e = np.maximum(e, -126.0)
+        return np.ldexp(1.0, (e - 8).astype(np.int64))
+    e = np.maximum(e, -14.0)
+    return np.ldexp(1.0, (e - 11).astype(np.int64))
+
+
+def assert_attention_close(got, ref, what="", out_dtype=W.F16):
+    """|got - ref| <= 2e-3 + 2e-3 |ref| elementwise for the kernel's fp32
+    result; the output is that result rounded once to fp16 / bf16, so the
+    check allows that rounding (half an ulp of the output type) on top."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), "%s: non-finite output" % what
     err = np.abs(got - ref)
-    bound = ATOL + RTOL * np.abs(ref)
+    bound = ATOL + RTOL * np.abs(ref) + half_ulp(ref, out_dtype)
     bad = err > bound
     if bad.any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)

@@ -55,7 +55,7 @@ def test_workload_end_to_end(name):
     out = g.decode()
     ref = o.decode()
     torch.cuda.synchronize()
-    H.assert_attention_close(H.out_to_double(out), ref, name)
+    H.assert_attention_close(H.out_to_double(out), ref, name, w.io_dtype)
     assert int(g.dev_err.item()) == 0
 
 
@@ -128,7 +128,7 @@ def test_decode_shapes(cdt, qdt, D, BS, G):
         out, err, _ = _gpu_decode(kc, vc, cdt, q, qdt, bt, ctxa, scale, ks, vs, partition_size=ps)
         ref = oracle.paged_attention_decode(kc, vc, cdt, q, qdt, bt, ctxa, scale, ks, vs)
         H.assert_attention_close(H.out_to_double(out), ref,
-                                 "shape %s partition %d" % ((cdt, qdt, D, BS, G), ps))
+                                 "shape %s partition %d" % ((cdt, qdt, D, BS, G), ps), qdt)
         assert err == 0
 
 
@@ -165,8 +165,8 @@ def test_e4m3_decode_table_through_the_kernel():
     ref = oracle.decode(oracle.E4M3, codes)
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(got), nan)
+    # equal values (the sign of a zero output is not defined by the sum)
     assert np.array_equal(got[~nan], ref[~nan])
-    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
 
 
 def test_empty_context_gives_zero_and_padding_is_ignored():
@@ -176,7 +176,7 @@ def test_empty_context_gives_zero_and_padding_is_ignored():
     out, err, _ = _gpu_decode(kc, vc, W.F16, q, W.F16, bt, ctx, 0.2, max_ctx=64)
     got = H.out_to_double(out)
     assert np.all(got[0] == 0) and np.all(got[2] == 0)
-    ref = oracle.paged_attention_decode(kc, vc, W.F16, q, W.F16, bt[1:2], ctx[1:2], 0.2)
+    ref = oracle.paged_attention_decode(kc, vc, W.F16, q[1:2], W.F16, bt[1:2], ctx[1:2], 0.2)
     H.assert_attention_close(got[1:2], ref, "empty neighbours")
     assert err == 0
 
@@ -191,7 +191,7 @@ def test_partition_boundaries(G, cdt):
     ks, vs = (0.05, 0.04) if cdt == W.E4M3 else (1.0, 1.0)
     out, err, _ = _gpu_decode(kc, vc, cdt, q, qdt, bt, ctxa, 0.09, ks, vs, partition_size=P)
     ref = oracle.paged_attention_decode(kc, vc, cdt, q, qdt, bt, ctxa, 0.09, ks, vs)
-    H.assert_attention_close(H.out_to_double(out), ref, "partitions")
+    H.assert_attention_close(H.out_to_double(out), ref, "partitions", qdt)
     assert err == 0
 
 
