@@ -58,7 +58,8 @@ typedef enum pkv_status {
     PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or count  */
     PKV_ERR_UNSUPPORTED = 2,   /* shape or type combination not implemented   */
     PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required  */
-    PKV_ERR_CUDA = 4           /* a kernel launch failed                      */
+    PKV_ERR_CUDA = 4,          /* a kernel launch failed                      */
+    PKV_ERR_SCRATCH_LIMIT = 5  /* request exceeds the static decode scratch   */
 } pkv_status;
 
 typedef enum pkv_dtype {
@@ -211,6 +212,44 @@ pkv_status pkv_lse_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
                           int32_t partition_size, const void* workspace,
                           size_t workspace_bytes, int32_t out_dtype, void* out,
                           pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_attention_decode_static_ws -- the decode above for callers that
+ * cannot allocate device memory.  The pages have no counterpart: this is a
+ * deployment convenience of the library, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc or pass a workspace: an engine that has
+ * reserved nearly all of the GPU's memory up front for its own KV-cache pool
+ * (a cudaMalloc would then fail), or code on a latency-critical path where
+ * cudaMalloc / cudaFree may synchronise the device.  This entry point takes
+ * the split-context partials from a static device array of
+ * PKV_STATIC_SCRATCH_BYTES inside the library and allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * Arguments and results: those of pkv_paged_attention_decode, without the
+ * workspace.  The caller still owns and passes q, the tables, dev_err, out.
+ * - Limit: a request with pkv_decode_workspace_bytes(...) above
+ *   PKV_STATIC_SCRATCH_BYTES returns PKV_ERR_SCRATCH_LIMIT and launches nothing.
+ * - Every GPU that loads the library holds the array until the process exits.
+ * - The first call on a device, with that device current, looks up the array's
+ *   device address (cudaGetSymbolAddress) and caches it for later calls; make
+ *   that first call before any stream capture.
+ * - All calls share the one array, which keeps the last call's contents.
+ *   Nothing in it needs to start at zero: each call writes every partial it
+ *   reads.  Calls whose kernels can overlap on the GPU (different streams,
+ *   different host threads) race on the array; issue them on one stream.
+ * ------------------------------------------------------------------------- */
+#define PKV_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+pkv_status pkv_paged_attention_decode_static_ws(const pkv_cache_desc* cache,
+                                                const void* q, int32_t q_dtype,
+                                                int32_t num_seqs, int32_t num_heads,
+                                                const int32_t* block_tables,
+                                                int32_t max_blocks_per_seq,
+                                                const int32_t* context_lens,
+                                                int32_t max_context_len, float scale,
+                                                int32_t partition_size, int32_t* dev_err,
+                                                void* out, pkv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -21,6 +21,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "pkv.h")
 
 PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+PKV_ERR_SCRATCH_LIMIT = 5
+PKV_STATIC_SCRATCH_BYTES = 32 << 20
 PKV_DEVERR_SLOT, PKV_DEVERR_BLOCK_ID, PKV_DEVERR_CONTEXT, PKV_DEVERR_COPY_PAIR = 1, 2, 4, 8
 
 
@@ -67,6 +69,8 @@ def load():
         "pkv_paged_attention_partitions": (i32, [dp, vp, i32, i32, i32, vp, i32, vp, i32, f32,
                                                  i32, vp, ctypes.c_size_t, vp, vp, vp]),
         "pkv_lse_reduce": (i32, [i32, i32, i32, vp, i32, i32, vp, ctypes.c_size_t, i32, vp, vp]),
+        "pkv_paged_attention_decode_static_ws": (i32, [dp, vp, i32, i32, i32, vp, i32, vp, i32,
+                                                       f32, i32, vp, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -211,4 +215,28 @@ def pkv_lse_reduce(num_seqs, num_heads, head_dim, context_lens, max_context_len,
                                  int(max_context_len), int(partition_size), _ptr(workspace),
                                  ws_bytes, dtype_code(out.dtype), _ptr(out), _stream(stream)),
            "pkv_lse_reduce")
+    return out
+
+
+def pkv_paged_attention_decode_static_ws(cache, q, block_tables, context_lens, max_context_len,
+                                         scale, partition_size=0, dev_err=None, out=None,
+                                         stream=None):
+    """Decode without a caller workspace: for callers that cannot allocate
+    device memory (an engine that has reserved the GPU's memory for its own
+    cache pool, or a latency-critical path where cudaMalloc may synchronise).
+    The partials live in the library's static 32 MiB device array; calls that
+    overlap on the GPU race on it, so keep them on one stream."""
+    _dense(q, "q")
+    _dense(block_tables, "block_tables")
+    _dense(context_lens, "context_lens")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    s, h, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().pkv_paged_attention_decode_static_ws(
+        ctypes.byref(cache), _ptr(q), dtype_code(q.dtype), s, h, _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale),
+        int(partition_size), _ptr(dev_err), _ptr(out), _stream(stream)),
+        "pkv_paged_attention_decode_static_ws")
     return out

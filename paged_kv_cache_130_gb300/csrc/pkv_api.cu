@@ -198,6 +198,8 @@ const char* pkv_status_string(int32_t status)
     case PKV_ERR_UNSUPPORTED: return "unsupported shape or type";
     case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case PKV_ERR_CUDA: return "CUDA launch failed";
+    case PKV_ERR_SCRATCH_LIMIT:
+        return "request exceeds the library's static decode scratch (PKV_STATIC_SCRATCH_BYTES)";
     default: return "unknown status";
     }
 }
