@@ -3,8 +3,10 @@
 One step = the whole hot path over one batch: the copy-on-write block copies
 (when the workload has any), the append of the step's new tokens, and decode
 attention over every sequence (partition kernel + log-sum-exp reduce).  The
-cache is pre-filled once (untimed).  Between timed steps L2 is flushed by a
-512 MiB device write; the decode inputs are also larger than L2.
+cache is pre-filled once (untimed).  Each stage is captured once as a CUDA
+graph; the timed loop replays the graphs between CUDA events.  The decode
+inputs of every benchmark layer exceed the 129 MB L2, so no flush is needed
+(``--flush write`` adds a 512 MiB write between steps).
 
 Output: one JSON line on rank 0.  ``value`` is decode KV-read GB/s: algorithmic
 bytes of one decode (every cached K/V element once per KV head, q, out, the used
@@ -57,6 +59,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true")
+    ap.add_argument("--flush", default="none", choices=["none", "write"],
+                    help="none: the decode inputs alone exceed L2; write: also write "
+                         "512 MiB between steps")
     return ap.parse_args(argv)
 
 
@@ -69,10 +75,24 @@ def dist_env():
     return world, rank, local
 
 
-def aggregate(values_by_rank_time, units):
-    """value = units summed over ranks / slowest rank's time."""
-    t = max(values_by_rank_time)
-    return sum(units) / t if t > 0 else 0.0
+def slowest(seconds, device=None):
+    """Each timing maximised over the ranks of the default process group
+    (unchanged when there is no group).  `device` is where the reduction
+    tensor lives: the rank's GPU under NCCL, the CPU under gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in seconds]
+    t = torch.tensor([float(x) for x in seconds], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_rate(units_per_rank, seconds_slowest, world):
+    """Replicas: every rank processes the same units; the job rate is all the
+    ranks' units over the slowest rank's time."""
+    return units_per_rank * world / seconds_slowest if seconds_slowest > 0 else 0.0
 
 
 # ------------------------------------------------------------------ clocks
@@ -240,7 +260,7 @@ def workload_config(w):
             "max_context_len": w.max_context_len,
             "copy_pairs": int(len(w.copy_pairs)),
             "step_tokens": int(len(w.step_slots)),
-            "l2": "flushed between steps by a 512 MiB write; decode inputs exceed the 129 MB L2",
+            "l2": "decode inputs exceed the 129 MB L2",
             "parallelism": "replicas"}
 
 
@@ -281,28 +301,52 @@ def run_gpu(args, w, prefill):
     step_k, step_v = dev16(sk), dev16(sv)
     step_slots = torch.from_numpy(w.step_slots).to(dev)
     pairs = torch.from_numpy(w.copy_pairs).to(dev) if len(w.copy_pairs) else None
-    ps = B.pkv_decode_partition_size(desc, w.partition_size)
+    ps = B.pkv_decode_partition_size(desc, w.num_heads, w.partition_size)
     ws_bytes = B.pkv_decode_workspace_bytes(desc, w.num_seqs, w.num_heads, w.max_context_len, ps)
     workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES if args.flush == "write" else 16, dtype=torch.uint8,
+                        device=dev)
     maxp = -(-w.max_context_len // ps)
     launches_per_step = 1 + (1 if pairs is not None else 0) + 1 + (1 if maxp > 1 else 0)
 
-    def step(ev=None):
+    def pre():
         if pairs is not None:
             B.pkv_copy_blocks(desc, pairs)
         B.pkv_kv_append(desc, step_k, step_v, step_slots)
-        if ev is not None:
-            ev.record()
+
+    def decode():
         B.pkv_paged_attention_decode(desc, q, bt, cl, w.max_context_len, w.scale,
                                      partition_size=ps, workspace=workspace, out=out)
 
+    def partitions():
+        B.pkv_paged_attention_partitions(desc, q, bt, cl, w.max_context_len, w.scale,
+                                         partition_size=ps, workspace=workspace, out=out)
+
+    def maybe_flush(i):
+        if args.flush == "write":
+            flush.fill_(i & 0xff)
+
     torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
+    for i in range(args.warmup):
+        maybe_flush(i)
+        pre()
+        decode()
+        partitions()
     torch.cuda.synchronize()
+
+    # Each stage is captured once as a CUDA graph and replayed: a replay costs
+    # the host a few microseconds, so the GPU never waits for Python between
+    # the events that bracket a stage.
+    stages = {"pre": pre, "decode": decode, "partitions": partitions}
+    replay = dict(stages)
+    if not args.no_graphs:
+        for name, fn in stages.items():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            replay[name] = g.replay
+        torch.cuda.synchronize()
 
     clocks = ClockSampler(local) if not args.no_clocks else None
     if clocks:
@@ -314,12 +358,14 @@ def run_gpu(args, w, prefill):
     t_wall0 = time.perf_counter()
     evs = []
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
+        maybe_flush(i)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e2 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        step(e1)
+        replay["pre"]()
+        e1.record()
+        replay["decode"]()
         e2.record()
         evs.append((e0, e1, e2))
     torch.cuda.synchronize()
@@ -333,12 +379,11 @@ def run_gpu(args, w, prefill):
     # the dominant kernel alone (partition kernel), for the roofline
     part_ms = []
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
+        maybe_flush(i)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        B.pkv_paged_attention_partitions(desc, q, bt, cl, w.max_context_len, w.scale,
-                                         partition_size=ps, workspace=workspace, out=out)
+        replay["partitions"]()
         b.record()
         part_ms.append((a, b))
     torch.cuda.synchronize()
@@ -348,12 +393,8 @@ def run_gpu(args, w, prefill):
     dec_s = sum(dec_ms) / 1e3
     step_s = sum(step_ms) / 1e3
     dbytes = w.decode_bytes()
-    if world > 1:
-        t = torch.tensor([dec_s, step_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dec_s, step_s = float(t[0]), float(t[1])
-    units = dbytes * args.steps * world
-    value = units / dec_s / 1e9
+    dec_s, step_s = slowest([dec_s, step_s], dev)
+    value = whole_job_rate(dbytes * args.steps, dec_s, world) / 1e9
 
     # end to end through the C ABI from pinned host buffers
     e2e = None
@@ -372,7 +413,7 @@ def run_gpu(args, w, prefill):
         d2h = h_out.numel() * h_out.element_size()
         e2e_ms = []
         for i in range(args.steps + args.warmup):
-            flush.fill_(i & 0xff)
+            maybe_flush(i)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
@@ -384,18 +425,16 @@ def run_gpu(args, w, prefill):
             cl.copy_(h_cl, non_blocking=True)
             if h_pairs is not None:
                 pairs.copy_(h_pairs, non_blocking=True)
-            step()
+            pre()
+            decode()
             h_out.copy_(out, non_blocking=True)
             b.record()
             b.synchronize()
             if i >= args.warmup:
                 e2e_ms.append(a.elapsed_time(b))
         e2e_s = sum(e2e_ms) / 1e3
-        if world > 1:
-            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t[0])
-        e2e = {"value": dbytes * args.steps * world / e2e_s / 1e9, "unit": "GB/s",
+        e2e_s = slowest([e2e_s], dev)[0]
+        e2e = {"value": whole_job_rate(dbytes * args.steps, e2e_s, world) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_s * 1e3 / args.steps}
 
@@ -411,11 +450,18 @@ def run_gpu(args, w, prefill):
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
+    cfg = workload_config(w)
+    cfg["l2"] = ("decode inputs (%.0f MB of K/V per step) exceed the 129 MB L2; no flush"
+                 % (w.kv_bytes() / 1e6) if args.flush == "none"
+                 else "512 MiB written between steps (L2 flush)")
+    cfg["timing"] = "CUDA events around CUDA-graph replays" if not args.no_graphs \
+        else "CUDA events around direct calls"
+    cfg["partition_size"] = ps
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(w),
+            "config": cfg,
             "hbm_frac": value / peak,
             "decode_ms": dec_s * 1e3 / args.steps,
             "decode_tokens_per_s": w.num_seqs * world * args.steps / dec_s,

@@ -17,7 +17,10 @@
  * Conventions shared by every call
  * --------------------------------
  * Ownership.  The caller owns every buffer.  The library never allocates,
- *   frees or synchronises; it keeps no state between calls and is thread-safe.
+ *   frees or synchronises, and it is thread-safe.  Between calls it keeps only
+ *   a per-device record of each decode kernel's launch size and a static
+ *   device table of work counters (one slot per in-flight decode launch, 1024
+ *   slots, each reset to zero by the launch that used it).
  * Pointers.   "device" pointers must be CUDA device (or managed) memory of
  *   the current device.  Element data (caches, q, k, v, out) must be 16-byte
  *   aligned and dense row-major in the shapes given.
@@ -74,6 +77,8 @@ typedef enum pkv_dtype {
 #define PKV_DEVERR_CONTEXT   4   /* context length < 0, above max_context_len  */
                                  /* or above max_blocks_per_seq * block_size   */
 #define PKV_DEVERR_COPY_PAIR 8   /* copy pair entry outside [0, num_blocks)    */
+#define PKV_DEVERR_TIMEOUT   16  /* a kernel's bounded wait on its own copies  */
+                                 /* ran out; that call's output is not valid   */
 
 /* One layer's cache.  k_cache / v_cache: device, caller-owned, layout above.
  * k_scale / v_scale: for an FP8 cache, the stored code times the scale is the
@@ -165,7 +170,11 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* caches, int32_t num_layers,
  * Launches: one partition kernel, then (when max_context_len exceeds one
  *   partition) the reduce kernel, chained with programmatic dependent launch.
  * ------------------------------------------------------------------------- */
-int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t requested);
+/* The partition size a decode with this cache and num_heads query heads uses:
+ * `requested` when positive, else the library's choice (about 256 KiB of K+V
+ * per KV head and partition, 1 MiB when query heads share KV heads). */
+int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t num_heads,
+                                  int32_t requested);
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
                                   int32_t num_heads, int32_t max_context_len,

@@ -13,121 +13,17 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include "decode_common.cuh"
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
 
-constexpr float kNegInf = -__builtin_huge_valf();
-
-__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
-
-// Where a partition CTA stands, decoded once at the top of every kernel.
-struct PartitionWork {
-    int s;
-    int part;
-    int t_begin;        // first token of the partition
-    int t_end;          // one past its last token
-    bool direct;        // context fits one partition: write out, no partials
-    bool zero_out;      // write zeros (empty or invalid context) and stop
-    bool zero_partial;  // write a neutral partial (table too short) and stop
-    bool idle;          // nothing to do
-};
-
-__device__ __forceinline__ PartitionWork locate(const DecodeParams& p, int s, int part)
-{
-    PartitionWork w{};
-    w.s = s;
-    w.part = part;
-    const int ctx = __ldg(p.context_lens + s);
-    const bool ctx_oob = ctx < 0 || ctx > p.max_context_len;
-    const bool table_short = !ctx_oob && ctx > p.max_blocks_per_seq * p.block_size;
-    if ((ctx_oob || table_short) && part == 0 && threadIdx.x == 0)
-        flag_error(p.dev_err, PKV_DEVERR_CONTEXT);
-    const int npart = ctx_oob ? 0 : ceil_div_i(ctx, p.partition_size);
-    w.direct = npart <= 1;
-    if (w.direct) {
-        w.idle = part != 0;
-        w.zero_out = !w.idle && (ctx_oob || table_short || ctx == 0);
-    } else {
-        w.idle = part >= npart;
-        w.zero_partial = !w.idle && table_short;
-    }
-    w.t_begin = part * p.partition_size;
-    w.t_end = min(ctx, w.t_begin + p.partition_size);
-    return w;
-}
-
-template <int QT>
-__device__ __forceinline__ void store_out(const DecodeParams& p, int s, int h, int d, float v)
-{
-    uint16_t* o = reinterpret_cast<uint16_t*>(p.out);
-    o[((int64_t)s * p.num_heads + h) * p.head_dim + d] = round_to<QT>(v);
-}
-
-// Writes for a CTA that has no attention to compute.
-template <int QT>
-__device__ void write_trivial(const DecodeParams& p, const PartitionWork& w, int head0, int nrows)
-{
-    const int D = p.head_dim;
-    for (int i = threadIdx.x; i < nrows * D; i += blockDim.x) {
-        const int h = head0 + i / D;
-        const int d = i % D;
-        if (w.zero_out) {
-            store_out<QT>(p, w.s, h, d, 0.f);
-        } else {
-            // neutral partial: contributes zero to the merged output
-            const int64_t prow = ((int64_t)w.s * p.num_heads + h) * p.max_partitions + w.part;
-            if (d == 0) {
-                p.ws_m[prow] = 0.f;
-                p.ws_l[prow] = 1.f;
-            }
-            p.ws_o[prow * D + d] = 0.f;
-        }
-    }
-}
-
-// Merge of the per-warp softmax states of `nrows` query heads and the CTA's
-// write.  sm_m / sm_l: [NW][ROWS]; sm_acc: [NW][ROWS][D] (v still unscaled).
-template <int QT, int NW, int ROWS>
-__device__ void finish_rows(const DecodeParams& p, const PartitionWork& w, int head0, int nrows,
-                            const float* sm_m, const float* sm_l, const float* sm_acc)
-{
-    const int D = p.head_dim;
-    for (int i = threadIdx.x; i < nrows * D; i += blockDim.x) {
-        const int row = i / D;
-        const int d = i % D;
-        float M = kNegInf;
-#pragma unroll
-        for (int k = 0; k < NW; ++k)
-            M = fmaxf(M, sm_m[k * ROWS + row]);
-        float L = 0.f;
-        float O = 0.f;
-        if (M != kNegInf) {
-#pragma unroll
-            for (int k = 0; k < NW; ++k) {
-                const float mk = sm_m[k * ROWS + row];
-                if (mk != kNegInf) {
-                    const float f = exp2f(mk - M);
-                    L += sm_l[k * ROWS + row] * f;
-                    O += sm_acc[(k * ROWS + row) * D + d] * f;
-                }
-            }
-        }
-        const int h = head0 + row;
-        if (w.direct) {
-            store_out<QT>(p, w.s, h, d, L > 0.f ? (O / L) * p.v_scale : 0.f);
-        } else {
-            const int64_t prow = ((int64_t)w.s * p.num_heads + h) * p.max_partitions + w.part;
-            if (d == 0) {
-                p.ws_m[prow] = M;
-                p.ws_l[prow] = L;
-            }
-            p.ws_o[prow * D + d] = O * p.v_scale;
-        }
-    }
-}
+using dec::ceil_div_i;
+using dec::kNegInf;
+using dec::locate;
+using dec::PartitionWork;
 
 // =====================================================================
 // CUDA-core kernel: one query head per CTA.
@@ -163,11 +59,11 @@ __global__ void __launch_bounds__(NW * 32, 4) decode_simt_kernel(const DecodePar
 
     pdl_launch_dependents();
 
-    const PartitionWork w = locate(p, s, part);
+    const PartitionWork w = locate(p, s, part, threadIdx.x == 0);
     if (w.idle)
         return;
     if (w.zero_out || w.zero_partial) {
-        write_trivial<QT>(p, w, h, 1);
+        dec::write_trivial<QT>(p, w, h, 1, threadIdx.x, blockDim.x);
         return;
     }
 
@@ -298,7 +194,7 @@ __global__ void __launch_bounds__(NW * 32, 4) decode_simt_kernel(const DecodePar
         sm_l[warp] = l_run;
     }
     __syncthreads();
-    finish_rows<QT, NW, ROWS>(p, w, h, 1, sm_m, sm_l, sm_acc);
+    dec::finish_rows<QT, NW, ROWS>(p, w, h, 1, sm_m, sm_l, sm_acc, threadIdx.x, blockDim.x);
 }
 
 // =====================================================================
@@ -378,11 +274,11 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_mma_kernel(const DecodePara
 
     pdl_launch_dependents();
 
-    const PartitionWork w = locate(p, s, part);
+    const PartitionWork w = locate(p, s, part, threadIdx.x == 0);
     if (w.idle)
         return;
     if (w.zero_out || w.zero_partial) {
-        write_trivial<CT>(p, w, head0, G);
+        dec::write_trivial<CT>(p, w, head0, G, threadIdx.x, blockDim.x);
         return;
     }
 
@@ -606,12 +502,16 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_mma_kernel(const DecodePara
             sm_acc[(warp * ROWS + row) * D + d] = acc[j][e];
         }
     __syncthreads();
-    finish_rows<CT, NW, ROWS>(p, w, head0, G, sm_m, sm_l, sm_acc);
+    dec::finish_rows<CT, NW, ROWS>(p, w, head0, G, sm_m, sm_l, sm_acc, threadIdx.x,
+                                   blockDim.x);
 }
 
 // ------------------------------------------------------------------ dispatch
 
 constexpr int kWarps = 4;
+// The persistent streaming kernel (decode_stream.cu) serves every shape; the
+// one-CTA-per-item kernels above remain as the simpler reference design.
+constexpr bool kUseOneCtaPerItem = false;
 
 template <int CT, int QT, int D, int BS>
 cudaError_t run_simt(const DecodeParams& p, dim3 grid, cudaStream_t stream)
@@ -706,6 +606,8 @@ cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream)
     if (ctas > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)ctas);
+    if (!kUseOneCtaPerItem)
+        return launch_decode_stream(p, mma, stream);
     if (mma) {
         return p.cache_dtype == kF16 ? mma_shape<kF16>(p, grid, stream)
                                      : mma_shape<kBF16>(p, grid, stream);

@@ -2,11 +2,13 @@
 //
 // For every (sequence, query head) whose context spans two or more
 // partitions: M = max_p m_p, w_p = 2^(m_p - M),
-// out = sum_p w_p o_p / sum_p w_p l_p.  One CTA per (s, h), one thread per
-// output dim; the per-partition weights go through shared memory.  Launched
-// with programmatic dependent launch: the prologue (index math, context
-// length) overlaps the partition kernel's tail, and griddepcontrol.wait orders
-// the partial reads after that kernel's writes.
+// out = sum_p w_p o_p / sum_p w_p l_p.
+// One warp per (sequence, head) row: lanes read the row's m and l strided,
+// reduce M and the weighted l with shuffles, then every lane accumulates its
+// D/32 output dims over the partitions with independent vector loads.
+// Launched with programmatic dependent launch: the context length is read
+// before griddepcontrol.wait (it is an input, not a partial), the partials
+// after it.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -16,86 +18,95 @@
 namespace pkv {
 namespace {
 
-constexpr int kReduceThreads = 128;
-constexpr int kMaxCachedParts = 512;      // weights kept in shared memory
+constexpr int kRowsPerCta = 4;
 
-template <int QT>
-__global__ void __launch_bounds__(kReduceThreads) lse_reduce_kernel(const ReduceParams p)
+template <int QT, int D>
+__global__ void __launch_bounds__(kRowsPerCta * 32) lse_reduce_kernel(const ReduceParams p)
 {
-    __shared__ float sm_w[kMaxCachedParts];
-    __shared__ float sm_red[kReduceThreads / 32];
-    __shared__ float sm_inv_l;
-
-    const int row = blockIdx.x;                       // s * num_heads + h
-    const int s = row / p.num_heads;
-    const int ctx = __ldg(p.context_lens + s);
-    if (ctx < 0 || ctx > p.max_context_len)
-        return;
-    const int npart = (ctx + p.partition_size - 1) / p.partition_size;
+    constexpr int DPL = D / 32;                       // dims per lane (2 or 4)
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+    const bool live = row < (int64_t)p.num_seqs * p.num_heads;
+    int npart = 0;
+    if (live) {
+        const int ctx = __ldg(p.context_lens + row / p.num_heads);
+        if (ctx >= 0 && ctx <= p.max_context_len)
+            npart = (ctx + p.partition_size - 1) / p.partition_size;
+    }
+    pdl_wait_primary();
     if (npart <= 1)
         return;
 
-    pdl_wait_primary();
-
-    const int64_t base = (int64_t)row * p.max_partitions;
+    const int64_t base = row * p.max_partitions;
     const float* m = p.ws_m + base;
     const float* l = p.ws_l + base;
-
-    // M = max_p m_p
-    float mx = -CUDART_INF_F;
-    for (int i = threadIdx.x; i < npart; i += blockDim.x)
-        mx = fmaxf(mx, m[i]);
+    float M = -CUDART_INF_F;
+    for (int i = lane; i < npart; i += 32)
+        M = fmaxf(M, m[i]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if ((threadIdx.x & 31) == 0)
-        sm_red[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    float M = sm_red[0];
-#pragma unroll
-    for (int i = 1; i < kReduceThreads / 32; ++i)
-        M = fmaxf(M, sm_red[i]);
-    __syncthreads();
-
-    // weights and their l-weighted sum
-    float lsum = 0.f;
-    for (int i = threadIdx.x; i < npart; i += blockDim.x) {
-        const float wi = (M == -CUDART_INF_F || m[i] == -CUDART_INF_F) ? 0.f : exp2f(m[i] - M);
-        if (i < kMaxCachedParts)
-            sm_w[i] = wi;
-        lsum += wi * l[i];
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int i = lane; i < npart; i += 32) {
+        const float mi = m[i];
+        if (M != -CUDART_INF_F && mi != -CUDART_INF_F)
+            L += exp2f(mi - M) * l[i];
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    if ((threadIdx.x & 31) == 0)
-        sm_red[threadIdx.x >> 5] = lsum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float L = 0.f;
-#pragma unroll
-        for (int i = 0; i < kReduceThreads / 32; ++i)
-            L += sm_red[i];
-        sm_inv_l = L > 0.f ? 1.f / L : 0.f;
-    }
-    __syncthreads();
-    const float inv_l = sm_inv_l;
+        L += __shfl_xor_sync(0xffffffffu, L, off);
 
-    const int D = p.head_dim;
-    uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + (int64_t)row * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        const float* o = p.ws_o + base * D + d;
-        float acc = 0.f;
-        for (int i = 0; i < npart; ++i) {
-            const float wi = i < kMaxCachedParts
-                                 ? sm_w[i]
-                                 : ((M == -CUDART_INF_F || m[i] == -CUDART_INF_F)
-                                        ? 0.f : exp2f(m[i] - M));
-            if (wi != 0.f)
-                acc = fmaf(wi, o[(int64_t)i * D], acc);
+    float acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e)
+        acc[e] = 0.f;
+    const float* o = p.ws_o + base * D + lane * DPL;
+    for (int c0 = 0; c0 < npart; c0 += 32) {
+        // weight of partition c0 + lane, then broadcast one by one
+        const int i = c0 + lane;
+        float wl = 0.f;
+        if (i < npart) {
+            const float mi = m[i];
+            wl = (M == -CUDART_INF_F || mi == -CUDART_INF_F) ? 0.f : exp2f(mi - M);
         }
-        out[d] = round_to<QT>(acc * inv_l);
+        const int n = min(32, npart - c0);
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wl, j);
+            const float* oj = o + (int64_t)(c0 + j) * D;
+            if constexpr (DPL == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(oj);
+                acc[0] = fmaf(wj, v.x, acc[0]);
+                acc[1] = fmaf(wj, v.y, acc[1]);
+                acc[2] = fmaf(wj, v.z, acc[2]);
+                acc[3] = fmaf(wj, v.w, acc[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(oj);
+                acc[0] = fmaf(wj, v.x, acc[0]);
+                acc[1] = fmaf(wj, v.y, acc[1]);
+            }
+        }
     }
+    const float inv_l = L > 0.f ? 1.f / L : 0.f;
+    uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * D + lane * DPL;
+    if constexpr (DPL == 4) {
+        const uint32_t w0 = pack2(round_to<QT>(acc[0] * inv_l), round_to<QT>(acc[1] * inv_l));
+        const uint32_t w1 = pack2(round_to<QT>(acc[2] * inv_l), round_to<QT>(acc[3] * inv_l));
+        *reinterpret_cast<uint2*>(out) = make_uint2(w0, w1);
+    } else {
+        *reinterpret_cast<uint32_t*>(out) =
+            pack2(round_to<QT>(acc[0] * inv_l), round_to<QT>(acc[1] * inv_l));
+    }
+}
+
+template <int QT>
+cudaError_t launch_typed(const ReduceParams& p, cudaLaunchConfig_t& cfg)
+{
+    if (p.head_dim == 128)
+        return cudaLaunchKernelEx(&cfg, lse_reduce_kernel<QT, 128>, p);
+    if (p.head_dim == 64)
+        return cudaLaunchKernelEx(&cfg, lse_reduce_kernel<QT, 64>, p);
+    return cudaErrorNotSupported;
 }
 
 }  // namespace
@@ -105,11 +116,12 @@ cudaError_t launch_lse_reduce(const ReduceParams& p, cudaStream_t stream, bool p
     const int64_t rows = (int64_t)p.num_seqs * p.num_heads;
     if (rows <= 0 || p.max_partitions <= 1)
         return cudaSuccess;
-    if (rows > 0x7fffffffLL)
+    const int64_t ctas = (rows + kRowsPerCta - 1) / kRowsPerCta;
+    if (ctas > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)rows);
-    cfg.blockDim = dim3(kReduceThreads);
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kRowsPerCta * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -118,9 +130,9 @@ cudaError_t launch_lse_reduce(const ReduceParams& p, cudaStream_t stream, bool p
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     if (p.out_dtype == kF16)
-        return cudaLaunchKernelEx(&cfg, lse_reduce_kernel<kF16>, p);
+        return launch_typed<kF16>(p, cfg);
     if (p.out_dtype == kBF16)
-        return cudaLaunchKernelEx(&cfg, lse_reduce_kernel<kBF16>, p);
+        return launch_typed<kBF16>(p, cfg);
     return cudaErrorNotSupported;
 }
 

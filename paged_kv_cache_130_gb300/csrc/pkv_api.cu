@@ -72,13 +72,17 @@ WorkspaceLayout layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
     return w;
 }
 
-int32_t resolve_partition(const pkv_cache_desc* c, int32_t requested)
+int32_t resolve_partition(const pkv_cache_desc* c, int32_t num_heads, int32_t requested)
 {
     if (requested > 0)
         return requested;
-    // about 128 KiB of K+V per partition of one KV head
+    // K+V bytes of one KV head per partition: 256 KiB when every query head
+    // has its own KV head, 1 MiB when a group of query heads shares it (one
+    // work item then serves the whole group)
     const int32_t elem = c->cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
-    int32_t tokens = (int32_t)(131072 / (2 * c->head_dim * elem));
+    const bool grouped = c->num_kv_heads > 0 && num_heads > c->num_kv_heads;
+    const int64_t budget = grouped ? (1 << 20) : (1 << 18);
+    int32_t tokens = (int32_t)(budget / (2 * c->head_dim * elem));
     tokens = tokens / c->block_size * c->block_size;
     return tokens < c->block_size ? c->block_size : tokens;
 }
@@ -285,11 +289,12 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* caches, int32_t num_layers,
     return PKV_OK;
 }
 
-int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t requested)
+int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t num_heads,
+                                  int32_t requested)
 {
     if (cache == nullptr || cache->block_size <= 0 || cache->head_dim <= 0)
         return 0;
-    return resolve_partition(cache, requested);
+    return resolve_partition(cache, num_heads, requested);
 }
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
@@ -299,7 +304,7 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
     if (cache == nullptr || cache->block_size <= 0 || cache->head_dim <= 0 || num_seqs <= 0 ||
         num_heads <= 0 || max_context_len <= 0 || partition_size < 0)
         return 0;
-    const int32_t part = resolve_partition(cache, partition_size);
+    const int32_t part = resolve_partition(cache, num_heads, partition_size);
     return (size_t)layout(num_seqs, num_heads, cache->head_dim, max_context_len, part).bytes;
 }
 
@@ -317,7 +322,7 @@ pkv_status pkv_paged_attention_partitions(const pkv_cache_desc* cache, const voi
                                   partition_size, out);
     if (st != PKV_OK || num_seqs == 0)
         return st;
-    const int32_t part = resolve_partition(cache, partition_size);
+    const int32_t part = resolve_partition(cache, num_heads, partition_size);
     const WorkspaceLayout wl = layout(num_seqs, num_heads, cache->head_dim, max_context_len, part);
     st = check_workspace(wl, workspace, workspace_bytes);
     if (st != PKV_OK)
@@ -362,7 +367,7 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, const void* q
                                   partition_size, out);
     if (st != PKV_OK || num_seqs == 0)
         return st;
-    const int32_t part = resolve_partition(cache, partition_size);
+    const int32_t part = resolve_partition(cache, num_heads, partition_size);
     const WorkspaceLayout wl = layout(num_seqs, num_heads, cache->head_dim, max_context_len, part);
     st = check_workspace(wl, workspace, workspace_bytes);
     if (st != PKV_OK)

@@ -84,6 +84,7 @@ struct CopyParams {
 
 // Each returns cudaSuccess, or cudaErrorNotSupported for a shape without a kernel.
 cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_stream(const DecodeParams& p, bool mma, cudaStream_t stream);
 cudaError_t launch_lse_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);

@@ -182,3 +182,30 @@ def gpu_available():
 
 def oracle_threads():
     return int(os.environ.get("PKV_ORACLE_THREADS", "0"))
+
+
+def segment_sequences(w, seg):
+    """Sequences whose tokens a prefill segment holds."""
+    if w.name == "cow_parallel_sampling_f16":
+        samples = w.num_seqs // int(w.notes["tails"].shape[0])
+        p = seg.key[1]
+        return set(range(p * samples, (p + 1) * samples))
+    return {seg.key[1]}
+
+
+def prefill_both(w, g, o, only=None, threads=8):
+    """Prefill the GPU cache with every segment and the oracle's cache with the
+    segments of `only` (all when None); values are drawn once, in parallel."""
+    import concurrent.futures as cf
+    segs = list(w.segments)
+    with cf.ThreadPoolExecutor(threads) as ex:
+        futs = [ex.submit(w.values, seg.key, len(seg.slots)) for seg in segs[:threads * 2]]
+        for i, seg in enumerate(segs):
+            k, v = futs[i].result()
+            futs[i] = None
+            j = i + threads * 2
+            if j < len(segs):
+                futs.append(ex.submit(w.values, segs[j].key, len(segs[j].slots)))
+            g.append(seg.slots, k, v)
+            if o is not None and (only is None or segment_sequences(w, seg) & set(only)):
+                o.append(seg.slots, k, v)

@@ -42,13 +42,14 @@ def test_status_strings(lib):
 
 def test_partition_size_and_workspace(lib):
     d = _desc()
-    assert B.pkv_decode_partition_size(d, 0) == 256          # 128 KiB of fp16 K+V
-    assert B.pkv_decode_partition_size(d, 64) == 64
+    assert B.pkv_decode_partition_size(d, 8, 0) == 512       # 256 KiB of fp16 K+V
+    assert B.pkv_decode_partition_size(d, 64, 0) == 2048     # grouped heads: 1 MiB
+    assert B.pkv_decode_partition_size(d, 8, 64) == 64
     f8 = _desc(cache_dtype=B.PKV_FP8_E4M3, block_size=32)
-    assert B.pkv_decode_partition_size(f8, 0) == 512
+    assert B.pkv_decode_partition_size(f8, 8, 0) == 1024
     # a context within one partition needs no workspace
-    assert B.pkv_decode_workspace_bytes(d, 4, 8, 256, 0) == 0
-    s, h, p, dim = 3, 8, 3, 128
+    assert B.pkv_decode_workspace_bytes(d, 4, 8, 512, 0) == 0
+    s, h, p, dim = 3, 8, 2, 128
     ml = -(-4 * s * h * p // 256) * 256
     want = 2 * ml + -(-4 * s * h * p * dim // 256) * 256
     assert B.pkv_decode_workspace_bytes(d, s, h, 700, 0) == want
@@ -89,7 +90,7 @@ def test_decode_host_checks(lib, fn):
     assert _decode(lib, d, out=0x6002, fn=fn) == B.PKV_ERR_INVALID_ARG
     assert _decode(lib, d, ctx=0, fn=fn) == B.PKV_ERR_INVALID_ARG
     assert _decode(lib, _desc(head_dim=80), fn=fn) == B.PKV_ERR_UNSUPPORTED
-    # three partitions need a workspace
+    # two partitions need a workspace
     assert _decode(lib, d, maxctx=700, fn=fn) == B.PKV_ERR_WORKSPACE
     assert _decode(lib, d, maxctx=700, ws=0x100010, ws_bytes=1 << 20, fn=fn) == \
         B.PKV_ERR_WORKSPACE                                              # misaligned
