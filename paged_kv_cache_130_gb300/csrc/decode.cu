@@ -509,8 +509,8 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_mma_kernel(const DecodePara
 // ------------------------------------------------------------------ dispatch
 
 constexpr int kWarps = 4;
-// The persistent streaming kernel (decode_stream.cu) serves every shape; the
-// one-CTA-per-item kernels above remain as the simpler reference design.
+// The persistent streaming kernel (decode_stream.cu) serves single-head work
+// items; grouped heads use the one-CTA-per-item tensor-core kernel above.
 constexpr bool kUseOneCtaPerItem = false;
 
 template <int CT, int QT, int D, int BS>
@@ -606,8 +606,10 @@ cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream)
     if (ctas > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)ctas);
-    if (!kUseOneCtaPerItem)
-        return launch_decode_stream(p, mma, stream);
+    // one query head per item: the persistent streaming kernel; grouped
+    // heads: the one-CTA-per-item tensor-core kernel below
+    if (!kUseOneCtaPerItem && !mma)
+        return launch_decode_stream(p, false, stream);
     if (mma) {
         return p.cache_dtype == kF16 ? mma_shape<kF16>(p, grid, stream)
                                      : mma_shape<kBF16>(p, grid, stream);

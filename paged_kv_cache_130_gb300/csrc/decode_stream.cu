@@ -1,7 +1,8 @@
 // decode_stream.cu -- persistent, warp-specialised decode partition kernel.
 //
-// The grid holds a few CTAs per SM.  Each CTA walks a static, strided list of
-// work items (partition, sequence, head unit).  One producer warp looks up each
+// The grid holds as many CTAs as fit on the GPU at once.  Work items are
+// (partition, sequence, query head); the CTAs' producer warps claim them from
+// a device counter, longest contexts first.  One producer warp looks up each
 // block through the block table (「KV 缓存与分页注意力」 §07 块表) and streams the
 // whole (block, KV head) tile of K and of V -- one contiguous run each -- into
 // a shared-memory ring with cp.async.bulk, signalling an mbarrier per stage.
@@ -226,416 +227,10 @@ struct SimtTile {
     }
 };
 
-// ------------------------------------------------------------------ tensor-core consumer
-
-__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1,
-                                         bool bf16)
-{
-    if (bf16) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    } else {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    }
-}
-
-__device__ __forceinline__ uint32_t word(const uint4& v, int i)
-{
-    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-
-// All G <= 16 query heads of one KV head against one tile, with
-// mma.sync m16n8k16 (fp32 accumulate), per 16-token sub-block:
-//   S = Q K^T : rows = query heads (padded to 16), 2 n-tiles of 8 tokens,
-//               k-steps over head_dim.  Inside each 32-wide slice head_dim is
-//               permuted (thread (r, c) holds dims 32s + 8c + 4u + {0,1},{2,3}
-//               for k-step 2s + u) identically for Q and K, so every fragment
-//               register comes from one 16-byte read and no dot changes.
-//   O += P V : A = P from the S accumulators (rows = heads, k = tokens);
-//               output column n of n-tile j is dim 64(j/8) + 8n + j%8, so the
-//               B values of one token come from one 16-byte read per 64 dims.
-// bf16 P is split into high and low bf16 parts (two MMAs, ~16 bits kept);
-// fp16 P is used directly.  Tokens past the context get p = 0 and their V is
-// cleared, so unwritten slots cannot reach the sums.
-template <int CT, int D, int BS, bool TWO_ROWS, int SK, int SV>
-struct MmaTile {
-    static constexpr bool kBf16 = (CT == kBF16);
-    static constexpr int NS = D / 32;
-    static constexpr int NH = D / 64;
-    static constexpr int NT = D / 8;
-    static_assert(BS % 16 == 0 && D % 64 == 0, "tile shape");
-
-    float acc[NT][4];
-    float m_a, m_b, l_a, l_b;        // rows r and r + 8 of this lane
-
-    __device__ __forceinline__ void reset()
-    {
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-            acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        m_a = m_b = kNegInf;
-        l_a = l_b = 0.f;
-    }
-
-    __device__ __forceinline__ void consume(const char* sk, const char* sv, const uint4* qa,
-                                            const uint4* qb, int lane, int tile_tok0, int t_end,
-                                            float qk)
-    {
-        const int r = lane >> 2;
-        const int c = lane & 3;
-#pragma unroll
-        for (int sb = 0; sb < BS / 16; ++sb) {
-            const int tb = tile_tok0 + sb * 16;
-            if (tb >= t_end)
-                break;
-            float sc[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-                for (int i2 = 0; i2 < NS; ++i2) {
-                    const uint4 kv = ld_shared_v4(sk + (sb * 16 + nt * 8 + r) * SK + (32 * i2 + 8 * c) * 2);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        uint32_t a[4];
-                        a[0] = word(qa[i2], 2 * u);
-                        a[2] = word(qa[i2], 2 * u + 1);
-                        if constexpr (TWO_ROWS) {
-                            a[1] = word(qb[i2], 2 * u);
-                            a[3] = word(qb[i2], 2 * u + 1);
-                        } else {
-                            a[1] = 0u;
-                            a[3] = 0u;
-                        }
-                        mma16816(sc[nt], a, word(kv, 2 * u), word(kv, 2 * u + 1), kBf16);
-                    }
-                }
-            }
-            // online softmax (base 2); element e of n-tile nt is token
-            // tb + nt*8 + 2c + (e & 1), row r (e < 2) or r + 8
-            // rows r + 8 exist only when the group has more than 8 heads
-            constexpr int NE = TWO_ROWS ? 4 : 2;
-            float x[2][4];
-            float mx_a = kNegInf, mx_b = kNegInf;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < NE; ++e) {
-                    const bool ok = tb + nt * 8 + 2 * c + (e & 1) < t_end;
-                    x[nt][e] = ok ? sc[nt][e] * qk : kNegInf;
-                    if (e < 2)
-                        mx_a = fmaxf(mx_a, x[nt][e]);
-                    else
-                        mx_b = fmaxf(mx_b, x[nt][e]);
-                }
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-            const float mn_a = fmaxf(m_a, mx_a);
-            const float al_a = exp2f(m_a - mn_a);
-            m_a = mn_a;
-            l_a *= al_a;
-            float mn_b = 0.f;
-            float al_b = 1.f;
-            if constexpr (TWO_ROWS) {
-                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-                mn_b = fmaxf(m_b, mx_b);
-                al_b = exp2f(m_b - mn_b);
-                m_b = mn_b;
-                l_b *= al_b;
-            }
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                acc[j][0] *= al_a;
-                acc[j][1] *= al_a;
-                if constexpr (TWO_ROWS) {
-                    acc[j][2] *= al_b;
-                    acc[j][3] *= al_b;
-                }
-            }
-            float pr[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (e >= NE) {
-                        pr[nt][e] = 0.f;
-                        continue;
-                    }
-                    const float mref = e < 2 ? mn_a : mn_b;
-                    pr[nt][e] = x[nt][e] == kNegInf ? 0.f : exp2f(x[nt][e] - mref);
-                    if (e < 2)
-                        l_a += pr[nt][e];
-                    else
-                        l_b += pr[nt][e];
-                }
-            // P fragments: a0 = row r n-tile 0, a1 = row r+8 n-tile 0,
-            // a2 = row r n-tile 1, a3 = row r+8 n-tile 1
-            uint32_t ph[4];
-            uint32_t pl[4];
-#pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) {
-                const int nt = q2 >> 1;
-                const int e0 = (q2 & 1) * 2;
-                const float v0 = pr[nt][e0], v1 = pr[nt][e0 + 1];
-                if constexpr (kBf16) {
-                    const uint16_t h0 = round_to<kBF16>(v0), h1 = round_to<kBF16>(v1);
-                    const float r0 = v0 - __uint_as_float((uint32_t)h0 << 16);
-                    const float r1 = v1 - __uint_as_float((uint32_t)h1 << 16);
-                    ph[q2] = pack2(h0, h1);
-                    pl[q2] = pack2(round_to<kBF16>(r0), round_to<kBF16>(r1));
-                } else {
-                    ph[q2] = pack2(round_to<kF16>(v0), round_to<kF16>(v1));
-                    pl[q2] = 0u;
-                }
-            }
-            // V rows of tokens 2c, 2c+1, 2c+8, 2c+9 (cleared past the context)
-            uint4 vv[4][NH];
-#pragma unroll
-            for (int tk = 0; tk < 4; ++tk) {
-                const int tok = 2 * c + (tk & 1) + 8 * (tk >> 1);
-                const bool ok = tb + tok < t_end;
-#pragma unroll
-                for (int hv = 0; hv < NH; ++hv)
-                    vv[tk][hv] = ok ? ld_shared_v4(sv + (sb * 16 + tok) * SV + (64 * hv + 8 * r) * 2)
-                                    : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const int hv = j / 8;
-                const int e = j % 8;
-                const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-                const uint32_t b0 = __byte_perm(word(vv[0][hv], e >> 1), word(vv[1][hv], e >> 1), sel);
-                const uint32_t b1 = __byte_perm(word(vv[2][hv], e >> 1), word(vv[3][hv], e >> 1), sel);
-                mma16816(acc[j], ph, b0, b1, kBf16);
-                if constexpr (kBf16)
-                    mma16816(acc[j], pl, b0, b1, kBf16);
-            }
-        }
-    }
-
-    // Row sums over the four lanes of a row group, then this warp's rows
-    // into shared memory: sm_m / sm_l [ROWS], sm_acc [ROWS][D] (rows < nrows).
-    __device__ __forceinline__ void store_warp(float* sm_m, float* sm_l, float* sm_acc, int lane,
-                                               int nrows)
-    {
-        const int r = lane >> 2;
-        const int c = lane & 3;
-        l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-        l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-        l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-        l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-        if (c == 0) {
-            if (r < nrows) {
-                sm_m[r] = m_a;
-                sm_l[r] = l_a;
-            }
-            if (r + 8 < nrows) {
-                sm_m[r + 8] = m_b;
-                sm_l[r + 8] = l_b;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = r + (e >> 1) * 8;
-                const int d = 64 * (j / 8) + 8 * (2 * c + (e & 1)) + (j % 8);
-                if (row < nrows)
-                    sm_acc[row * D + d] = acc[j][e];
-            }
-    }
-};
-
-// Grouped heads, G <= 8, tokens as the MMA rows (no padded rows):
-//   S^T = K Q^T : A = K (16 tokens x 16 dims per k-step), B = Q^T (8 heads);
-//                 the head_dim permutation inside each 32-wide slice is the
-//                 one above, so the K and Q reads are unchanged.
-//   O^T += V^T P: A = V^T (16 dims x 16 tokens), B = P (16 tokens x 8 heads).
-//                 P leaves the S^T accumulators as (token, head) pairs and is
-//                 transposed in registers with movmatrix.  Row r of m-tile j
-//                 is dim 8r + j, row r + 8 is dim 64 + 8r + j (head_dim 128)
-//                 or 8r + 4 + j (head_dim 64), so a thread's V values of one
-//                 token come from one 16-byte read per 64 dims.
-__device__ __forceinline__ uint32_t transpose8x8(uint32_t x)
-{
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
-template <int CT, int D, int BS>
-struct GqaTile {
-    static constexpr bool kBf16 = (CT == kBF16);
-    static constexpr int NS = D / 32;           // 32-wide slices: two k-steps each
-    static constexpr int NH = D / 64;           // 16-byte V reads per token
-    static constexpr int MT = D / 16;           // m-tiles of O^T
-    static_assert(BS % 16 == 0 && (D == 64 || D == 128), "tile shape");
-
-    float acc[MT][4];                           // (dim, head 2c | 2c+1) pairs
-    float m0, m1, l0, l1;                       // heads 2c and 2c+1 of this lane
-
-    __device__ __forceinline__ void reset()
-    {
-#pragma unroll
-        for (int j = 0; j < MT; ++j)
-            acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        m0 = m1 = kNegInf;
-        l0 = l1 = 0.f;
-    }
-
-    // qa: this lane's Q fragment slices of head r (zero past the group)
-    __device__ __forceinline__ void consume(const char* sk, const char* sv, const uint4* qa,
-                                            int lane, int tile_tok0, int t_end, float qk)
-    {
-        const int r = lane >> 2;
-        const int c = lane & 3;
-#pragma unroll
-        for (int sb = 0; sb < BS / 16; ++sb) {
-            const int tb = tile_tok0 + sb * 16;
-            if (tb >= t_end)
-                break;
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i2 = 0; i2 < NS; ++i2) {
-                const uint4 k0 = ld_shared_v4(sk + ((sb * 16 + r) * D + 32 * i2 + 8 * c) * 2);
-                const uint4 k1 = ld_shared_v4(sk + ((sb * 16 + r + 8) * D + 32 * i2 + 8 * c) * 2);
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const uint32_t a[4] = {word(k0, 2 * u), word(k1, 2 * u), word(k0, 2 * u + 1),
-                                           word(k1, 2 * u + 1)};
-                    mma16816(sc, a, word(qa[i2], 2 * u), word(qa[i2], 2 * u + 1), kBf16);
-                }
-            }
-            // sc[0], sc[1]: token tb + r, heads 2c, 2c+1; sc[2], sc[3]: token tb + r + 8
-            const bool ok0 = tb + r < t_end;
-            const bool ok1 = tb + r + 8 < t_end;
-            const float x00 = ok0 ? sc[0] * qk : kNegInf;
-            const float x01 = ok0 ? sc[1] * qk : kNegInf;
-            const float x10 = ok1 ? sc[2] * qk : kNegInf;
-            const float x11 = ok1 ? sc[3] * qk : kNegInf;
-            float mx0 = fmaxf(x00, x10);
-            float mx1 = fmaxf(x01, x11);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(m0, mx0);
-            const float mn1 = fmaxf(m1, mx1);
-            const float al0 = exp2f(m0 - mn0);
-            const float al1 = exp2f(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            const float p00 = ok0 ? exp2f(x00 - mn0) : 0.f;
-            const float p01 = ok0 ? exp2f(x01 - mn1) : 0.f;
-            const float p10 = ok1 ? exp2f(x10 - mn0) : 0.f;
-            const float p11 = ok1 ? exp2f(x11 - mn1) : 0.f;
-            l0 = l0 * al0 + p00 + p10;
-            l1 = l1 * al1 + p01 + p11;
-#pragma unroll
-            for (int j = 0; j < MT; ++j) {
-                acc[j][0] *= al0;
-                acc[j][1] *= al1;
-                acc[j][2] *= al0;
-                acc[j][3] *= al1;
-            }
-            // P as the B operand: transpose the (token, head) pairs per 8 tokens
-            uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
-            if constexpr (kBf16) {
-                const uint16_t h00 = round_to<kBF16>(p00), h01 = round_to<kBF16>(p01);
-                const uint16_t h10 = round_to<kBF16>(p10), h11 = round_to<kBF16>(p11);
-                bh0 = transpose8x8(pack2(h00, h01));
-                bh1 = transpose8x8(pack2(h10, h11));
-                const float r00 = p00 - __uint_as_float((uint32_t)h00 << 16);
-                const float r01 = p01 - __uint_as_float((uint32_t)h01 << 16);
-                const float r10 = p10 - __uint_as_float((uint32_t)h10 << 16);
-                const float r11 = p11 - __uint_as_float((uint32_t)h11 << 16);
-                bl0 = transpose8x8(pack2(round_to<kBF16>(r00), round_to<kBF16>(r01)));
-                bl1 = transpose8x8(pack2(round_to<kBF16>(r10), round_to<kBF16>(r11)));
-            } else {
-                bh0 = transpose8x8(pack2(round_to<kF16>(p00), round_to<kF16>(p01)));
-                bh1 = transpose8x8(pack2(round_to<kF16>(p10), round_to<kF16>(p11)));
-            }
-            // V rows of tokens 2c, 2c+1, 2c+8, 2c+9 (cleared past the context)
-            uint4 vv[4][NH];
-#pragma unroll
-            for (int tk = 0; tk < 4; ++tk) {
-                const int tok = 2 * c + (tk & 1) + 8 * (tk >> 1);
-                const bool ok = tb + tok < t_end;
-#pragma unroll
-                for (int hv = 0; hv < NH; ++hv)
-                    vv[tk][hv] = ok ? ld_shared_v4(sv + ((sb * 16 + tok) * D + 64 * hv + 8 * r) * 2)
-                                    : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int j = 0; j < MT; ++j) {
-                // row r: element j of the first read; row r + 8: element j of the
-                // second read (head_dim 128) or element j + 4 of the first
-                const int hb = NH == 2 ? 1 : 0;
-                const int eb = NH == 2 ? j : j + 4;
-                const uint32_t sa = (j & 1) ? 0x7632u : 0x5410u;
-                const uint32_t sb2 = (eb & 1) ? 0x7632u : 0x5410u;
-                uint32_t a[4];
-                a[0] = __byte_perm(word(vv[0][0], j >> 1), word(vv[1][0], j >> 1), sa);
-                a[1] = __byte_perm(word(vv[0][hb], eb >> 1), word(vv[1][hb], eb >> 1), sb2);
-                a[2] = __byte_perm(word(vv[2][0], j >> 1), word(vv[3][0], j >> 1), sa);
-                a[3] = __byte_perm(word(vv[2][hb], eb >> 1), word(vv[3][hb], eb >> 1), sb2);
-                mma16816(acc[j], a, bh0, bh1, kBf16);
-                if constexpr (kBf16)
-                    mma16816(acc[j], a, bl0, bl1, kBf16);
-            }
-        }
-    }
-
-    // Per-head sums over the lanes sharing c, then this warp's rows into
-    // shared memory: sm_m / sm_l [8], sm_acc [8][D] (heads < nrows).
-    __device__ __forceinline__ void store_warp(float* sm_m, float* sm_l, float* sm_acc, int lane,
-                                               int nrows)
-    {
-        const int r = lane >> 2;
-        const int c = lane & 3;
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-        }
-        if (r == 0) {
-            if (2 * c < nrows) {
-                sm_m[2 * c] = m0;
-                sm_l[2 * c] = l0;
-            }
-            if (2 * c + 1 < nrows) {
-                sm_m[2 * c + 1] = m1;
-                sm_l[2 * c + 1] = l1;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < MT; ++j) {
-            const int d0 = 8 * r + j;
-            const int d1 = NH == 2 ? 64 + 8 * r + j : 8 * r + 4 + j;
-            if (2 * c < nrows) {
-                sm_acc[(2 * c) * D + d0] = acc[j][0];
-                sm_acc[(2 * c) * D + d1] = acc[j][2];
-            }
-            if (2 * c + 1 < nrows) {
-                sm_acc[(2 * c + 1) * D + d0] = acc[j][1];
-                sm_acc[(2 * c + 1) * D + d1] = acc[j][3];
-            }
-        }
-    }
-};
-
 // ------------------------------------------------------------------ the kernel
 
 constexpr int kCtxCache = 512;        // context lengths kept in shared memory
+constexpr int kSortMax = 128;         // batches up to this size are taken longest first
 constexpr int kItemQueue = 4;         // work items the producer may publish ahead
 constexpr int kSchedSlots = 1024;     // launches that may be in flight at once
 
@@ -647,27 +242,20 @@ constexpr int kSchedSlots = 1024;     // launches that may be in flight at once
 __device__ unsigned int g_sched[kSchedSlots][2];
 
 // Stage geometry: each (block, KV head) tile lands as one contiguous run, one
-// bulk copy for K and one for V (a copy per token row instead would cost the
-// copy engine far more than the rows' bank conflicts cost the consumers).
-template <int CT, int D, int BS, int MODE>
+// bulk copy for K and one for V, in the tile's own byte order.
+template <int CT, int D, int BS>
 struct StreamShape {
-    static constexpr int ROW = D * Elem<CT>::bytes;           // bytes of one token row
-    static constexpr int TILE = BS * ROW;                     // one K (or V) tile in HBM
-    static constexpr int SK = ROW;                            // smem stride of K rows
-    static constexpr int SV = ROW;                            // smem stride of V rows
-    static constexpr int VOFF = BS * SK;                      // V rows start here
-    static constexpr int STAGE = ((BS * (SK + SV)) + 127) / 128 * 128;
-    // ring bytes: 64 KiB for the CUDA-core consumer; 48 KiB for the grouped-
-    // head consumer, whose merge rows and q slots are larger, so that three
-    // CTAs still fit on an SM
-    static constexpr int NSTG_RAW = (MODE ? 49152 : 65536) / STAGE;
+    static constexpr int TILE = BS * D * Elem<CT>::bytes;     // one K (or V) tile
+    static constexpr int VOFF = TILE;                         // V starts here
+    static constexpr int STAGE = (2 * TILE + 127) / 128 * 128;
+    static constexpr int NSTG_RAW = 65536 / STAGE;           // a 64 KiB ring
     static constexpr int NSTG = NSTG_RAW < 4 ? 4 : (NSTG_RAW > 16 ? 16 : NSTG_RAW);
 };
 
 // Shared-memory layout of one CTA, in bytes from the (128-aligned) base.
-template <int CT, int D, int BS, int NC, int MODE, int ROWS>
+template <int CT, int D, int BS, int NC>
 struct StreamSmem {
-    using S = StreamShape<CT, D, BS, MODE>;
+    using S = StreamShape<CT, D, BS>;
     static constexpr int ring = 0;
     static constexpr int full = ring + S::NSTG * S::STAGE;
     static constexpr int empty = full + 8 * S::NSTG;
@@ -678,22 +266,22 @@ struct StreamSmem {
     static constexpr int flags = cur + 8;
     static constexpr int abort = flags + 4 * S::NSTG;
     static constexpr int ctx = abort + 16;
-    static constexpr int QSLOT = ((ROWS * D * 2 + 127) / 128) * 128;   // q rows of one item
-    static constexpr int qbuf = ((ctx + 4 * kCtxCache + 127) / 128) * 128;
+    static constexpr int order = ctx + 4 * kCtxCache;
+    static constexpr int QSLOT = ((D * 2 + 127) / 128) * 128;   // q row of one item
+    static constexpr int qbuf = ((order + 4 * kSortMax + 127) / 128) * 128;
     static constexpr int merge_m = qbuf + kItemQueue * QSLOT;
-    static constexpr int merge_l = merge_m + 4 * NC * ROWS;
-    static constexpr int merge_acc = merge_l + 4 * NC * ROWS;
-    static constexpr int bytes = merge_acc + 4 * NC * ROWS * D;
+    static constexpr int merge_l = merge_m + 4 * NC;
+    static constexpr int merge_acc = merge_l + 4 * NC;
+    static constexpr int bytes = merge_acc + 4 * NC * D;
 };
 
-// MODE 0: one query head per item, CUDA-core consumer.
-// MODE 1: one KV head per item (its G <= ROWS query heads), tensor-core consumer.
-template <int CT, int QT, int D, int BS, int NC, int MODE, int ROWS>
+// One work item = one (partition, sequence, query head); CUDA-core consumer.
+template <int CT, int QT, int D, int BS, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32)
     decode_stream_kernel(const DecodeParams p, const int num_items, const int slot)
 {
-    using Shape = StreamShape<CT, D, BS, MODE>;
-    using L = StreamSmem<CT, D, BS, NC, MODE, ROWS>;
+    using Shape = StreamShape<CT, D, BS>;
+    using L = StreamSmem<CT, D, BS, NC>;
     constexpr int TILE = Shape::TILE;
     constexpr int NSTG = Shape::NSTG;
     constexpr int NCT = NC * 32;                      // consumer threads
@@ -709,6 +297,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     volatile int* flags = reinterpret_cast<volatile int*>(smem + L::flags);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort);
     int* sm_ctx = reinterpret_cast<int*>(smem + L::ctx);
+    int* sm_order = reinterpret_cast<int*>(smem + L::order);
     float* sm_m = reinterpret_cast<float*>(smem + L::merge_m);
     float* sm_l = reinterpret_cast<float*>(smem + L::merge_l);
     float* sm_acc = reinterpret_cast<float*>(smem + L::merge_acc);
@@ -732,9 +321,26 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     for (int i = threadIdx.x; i < ncache; i += blockDim.x)
         sm_ctx[i] = __ldg(p.context_lens + i);
     __syncthreads();
+    // Longest first: every CTA ranks the sequences by descending context
+    // length (ties by index) and walks work items in that order, so that the
+    // dynamic scheduler hands out the largest items first and the last ones
+    // to finish are short.
+    const bool sorted = p.num_seqs <= kSortMax;
+    if (sorted) {
+        for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
+            const int ci = sm_ctx[i];
+            int rank = 0;
+            for (int j = 0; j < p.num_seqs; ++j) {
+                const int cj = sm_ctx[j];
+                rank += (cj > ci) || (cj == ci && j < i);
+            }
+            sm_order[rank] = i;
+        }
+    }
+    __syncthreads();
     pdl_launch_dependents();
 
-    const int U = MODE ? p.num_kv_heads : p.num_heads;
+    const int U = p.num_heads;
     const int64_t block_stride = (int64_t)p.num_kv_heads * TILE;
 
     if (warp == NC) {
@@ -756,7 +362,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
             if (!last) {
                 u = item % U;
                 const int rest = item / U;
-                s = rest % p.num_seqs;
+                s = sorted ? sm_order[rest % p.num_seqs] : rest % p.num_seqs;
                 part = rest / p.num_seqs;
                 const int ctx = s < ncache ? sm_ctx[s] : __ldg(p.context_lens + s);
                 w = dec::locate_ctx(p, s, part, ctx, false);
@@ -775,8 +381,8 @@ __global__ void __launch_bounds__((NC + 1) * 32)
                         mbar_arrive(&iq_full[qs]);
                     } else {
                         // the item's query rows travel with its queue entry
-                        const int head0 = MODE ? u * p.group : u;
-                        const uint32_t qbytes = (MODE ? p.group : 1) * D * 2;
+                        const int head0 = u;
+                        const uint32_t qbytes = D * 2;
                         mbar_arrive_expect_tx(&iq_full[qs], qbytes);
                         bulk_load(qbuf + qs * L::QSLOT,
                                   reinterpret_cast<const char*>(p.q) +
@@ -791,7 +397,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
                 break;
             if (w.zero_out || w.zero_partial)
                 continue;                              // the consumers write it
-            const int g = MODE ? u : u / p.group;
+            const int g = u / p.group;
             const int nblk = ceil_div_i(w.t_end - w.t_begin, BS);
             const int32_t* table =
                 p.block_tables + (int64_t)s * p.max_blocks_per_seq + w.t_begin / BS;
@@ -882,12 +488,12 @@ __global__ void __launch_bounds__((NC + 1) * 32)
             break;
         const int u = item % U;
         const int rest = item / U;
-        const int s = rest % p.num_seqs;
+        const int s = sorted ? sm_order[rest % p.num_seqs] : rest % p.num_seqs;
         const int part = rest / p.num_seqs;
         const int ctx = s < ncache ? sm_ctx[s] : __ldg(p.context_lens + s);
         const PartitionWork w = dec::locate_ctx(p, s, part, ctx, ctid == 0);
-        const int head0 = MODE ? u * p.group : u;
-        const int nrows = MODE ? p.group : 1;
+        const int head0 = u;
+        const int nrows = 1;
         const int qs = n % kItemQueue;
         const unsigned char* qrow_s = qbuf + qs * L::QSLOT;
         if (w.zero_out || w.zero_partial) {
@@ -903,7 +509,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
         // entry is released below)
         __all_sync(0xffffffffu, wait_bounded(&iq_full[qs], (n / kItemQueue) & 1, abort_flag,
                                              p.dev_err));
-        if constexpr (MODE == 0) {
+        {
             using T = SimtTile<CT, D, BS>;
             T st;
             st.reset();
@@ -941,74 +547,13 @@ __global__ void __launch_bounds__((NC + 1) * 32)
                 sm_m[warp] = st.m;
                 sm_l[warp] = st.l;
             }
-        } else if constexpr (ROWS <= 8) {
-            using T = GqaTile<CT, D, BS>;
-            T st;
-            st.reset();
-            const int r = lane >> 2;
-            const int c = lane & 3;
-            uint4 qa[T::NS];
-#pragma unroll
-            for (int i = 0; i < T::NS; ++i)
-                qa[i] = r < nrows ? ld_shared_v4(qrow_s + (r * D + 32 * i + 8 * c) * 2)
-                                  : make_uint4(0, 0, 0, 0);
-            for (int k = k0; k < nblk; k += NC) {
-                const uint32_t tt = t + k;
-                const uint32_t stage = tt % NSTG;
-                const bool ok = __all_sync(0xffffffffu, wait_bounded(&full[stage], (tt / NSTG) & 1,
-                                                                    abort_flag, p.dev_err));
-                if (ok && flags[stage]) {
-                    const char* sk = reinterpret_cast<const char*>(ring + stage * Shape::STAGE);
-                    st.consume(sk, sk + Shape::VOFF, qa, lane, w.t_begin + k * BS, w.t_end, qk);
-                }
-                __syncwarp();
-                if (ok && lane == 0)
-                    mbar_arrive(&empty[stage]);
-            }
-            st.store_warp(sm_m + warp * ROWS, sm_l + warp * ROWS, sm_acc + warp * ROWS * D, lane,
-                          nrows);
-        } else {
-            constexpr bool kTwo = true;
-            using T = MmaTile<CT, D, BS, kTwo, Shape::SK, Shape::SV>;
-            T st;
-            st.reset();
-            const int r = lane >> 2;
-            const int c = lane & 3;
-            uint4 qa[T::NS];
-            uint4 qb[kTwo ? T::NS : 1];
-            {
-#pragma unroll
-                for (int i = 0; i < T::NS; ++i) {
-                    qa[i] = r < nrows ? ld_shared_v4(qrow_s + (r * D + 32 * i + 8 * c) * 2)
-                                      : make_uint4(0, 0, 0, 0);
-                    if constexpr (kTwo)
-                        qb[i] = r + 8 < nrows
-                                    ? ld_shared_v4(qrow_s + ((r + 8) * D + 32 * i + 8 * c) * 2)
-                                    : make_uint4(0, 0, 0, 0);
-                }
-            }
-            for (int k = k0; k < nblk; k += NC) {
-                const uint32_t tt = t + k;
-                const uint32_t stage = tt % NSTG;
-                const bool ok = __all_sync(0xffffffffu, wait_bounded(&full[stage], (tt / NSTG) & 1,
-                                                                    abort_flag, p.dev_err));
-                if (ok && flags[stage]) {
-                    const char* sk = reinterpret_cast<const char*>(ring + stage * Shape::STAGE);
-                    st.consume(sk, sk + Shape::VOFF, qa, qb, lane, w.t_begin + k * BS, w.t_end, qk);
-                }
-                __syncwarp();
-                if (ok && lane == 0)
-                    mbar_arrive(&empty[stage]);
-            }
-            st.store_warp(sm_m + warp * ROWS, sm_l + warp * ROWS, sm_acc + warp * ROWS * D, lane,
-                          nrows);
         }
         t += nblk;
         consumers_sync(NCT);
         // every consumer warp has its q in registers: the queue entry is free
         if (warp == 0 && lane == 0)
             mbar_arrive(&iq_empty[qs]);
-        dec::finish_rows<QT, NC, ROWS>(p, w, head0, nrows, sm_m, sm_l, sm_acc, ctid, NCT);
+        dec::finish_rows<QT, NC, 1>(p, w, head0, nrows, sm_m, sm_l, sm_acc, ctid, NCT);
     }
 }
 
@@ -1059,19 +604,19 @@ cudaError_t resident_ctas(LaunchCache& cache, Kern kern, int threads, int smem, 
     return cudaSuccess;
 }
 
-template <int CT, int QT, int D, int BS, int MODE, int ROWS>
+template <int CT, int QT, int D, int BS>
 cudaError_t run_stream(const DecodeParams& p, cudaStream_t stream)
 {
     constexpr int NC = 4;
-    using L = StreamSmem<CT, D, BS, NC, MODE, ROWS>;
-    auto kern = decode_stream_kernel<CT, QT, D, BS, NC, MODE, ROWS>;
+    using L = StreamSmem<CT, D, BS, NC>;
+    auto kern = decode_stream_kernel<CT, QT, D, BS, NC>;
     const int smem = L::bytes;
     static LaunchCache cache;
     int max_ctas = 0;
     cudaError_t e = resident_ctas(cache, kern, (NC + 1) * 32, smem, &max_ctas);
     if (e != cudaSuccess)
         return e;
-    const int64_t units = MODE ? p.num_kv_heads : p.num_heads;
+    const int64_t units = p.num_heads;
     const int64_t items = (int64_t)p.max_partitions * p.num_seqs * units;
     if (items <= 0)
         return cudaSuccess;
@@ -1087,9 +632,9 @@ template <int CT, int QT, int D>
 cudaError_t stream_simt_bs(const DecodeParams& p, cudaStream_t st)
 {
     switch (p.block_size) {
-    case 8:  return run_stream<CT, QT, D, 8, 0, 1>(p, st);
-    case 16: return run_stream<CT, QT, D, 16, 0, 1>(p, st);
-    case 32: return run_stream<CT, QT, D, 32, 0, 1>(p, st);
+    case 8:  return run_stream<CT, QT, D, 8>(p, st);
+    case 16: return run_stream<CT, QT, D, 16>(p, st);
+    case 32: return run_stream<CT, QT, D, 32>(p, st);
     default: return cudaErrorNotSupported;
     }
 }
@@ -1102,32 +647,15 @@ cudaError_t stream_simt(const DecodeParams& p, cudaStream_t st)
                                                  : cudaErrorNotSupported);
 }
 
-template <int CT, int D, int BS>
-cudaError_t stream_mma_rows(const DecodeParams& p, cudaStream_t st)
-{
-    return p.group <= 8 ? run_stream<CT, CT, D, BS, 1, 8>(p, st)
-                        : run_stream<CT, CT, D, BS, 1, 16>(p, st);
-}
-
-template <int CT>
-cudaError_t stream_mma(const DecodeParams& p, cudaStream_t st)
-{
-    if (p.head_dim == 64 && p.block_size == 16) return stream_mma_rows<CT, 64, 16>(p, st);
-    if (p.head_dim == 64 && p.block_size == 32) return stream_mma_rows<CT, 64, 32>(p, st);
-    if (p.head_dim == 128 && p.block_size == 16) return stream_mma_rows<CT, 128, 16>(p, st);
-    if (p.head_dim == 128 && p.block_size == 32) return stream_mma_rows<CT, 128, 32>(p, st);
-    return cudaErrorNotSupported;
-}
-
 }  // namespace
 
-// Streaming decode partitions; `mma` selects the grouped-head consumer.
+// Streaming decode partitions for single-head work items.  Grouped heads go to
+// the one-CTA-per-item tensor-core kernel (decode.cu): a grouped-head variant
+// of this kernel ended in GPU faults whose cause was not found, and is gone.
 cudaError_t launch_decode_stream(const DecodeParams& p, bool mma, cudaStream_t stream)
 {
-    if (mma) {
-        return p.cache_dtype == kF16 ? stream_mma<kF16>(p, stream)
-                                     : stream_mma<kBF16>(p, stream);
-    }
+    if (mma)
+        return cudaErrorNotSupported;
     if (p.cache_dtype == kF16)
         return stream_simt<kF16, kF16>(p, stream);
     if (p.cache_dtype == kBF16)
