@@ -40,13 +40,33 @@ MODEL_LAYERS = {"opt13b_f16": 40, "llama2_70b_bf16_gqa": 80, "llama2_7b_fp8_long
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch of the decode partition kernel from an ncu capture,
-# valid while csrc/decode.cu has the hash below (else reported as null)
-NCU_TRAFFIC = {}
+# valid while the decode kernel sources hash to "src_sha" (else reported as null)
+NCU_TRAFFIC = {
+    "opt13b_f16": {"bytes_per_launch": 366101760 + 3785728, "src_sha": "dc35b6044e43708b"},
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642911232 + 3888640,
+                            "src_sha": "dc35b6044e43708b"},
+    "cow_parallel_sampling_f16": {"bytes_per_launch": 747838208 + 3827200,
+                                  "src_sha": "dc35b6044e43708b"},
+}
+DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_common.cuh")
 
 
-def _sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def decode_src_sha():
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_130_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def decode_kernel_name(w):
+    """Which partition kernel the library runs for this workload: grouped
+    16-bit heads go to the tensor-core kernel, everything else streams."""
+    from paged_kv_cache_130_gb300 import workloads as W
+    group = w.num_heads // w.num_kv_heads
+    grouped = (2 <= group <= 16 and w.cache_dtype == w.io_dtype and w.cache_dtype != W.E4M3
+               and w.block_size % 16 == 0)
+    return "decode_mma_kernel" if grouped else "decode_stream_kernel"
 
 
 def parse_args(argv=None):
@@ -301,7 +321,8 @@ def run_gpu(args, w, prefill):
     step_k, step_v = dev16(sk), dev16(sv)
     step_slots = torch.from_numpy(w.step_slots).to(dev)
     pairs = torch.from_numpy(w.copy_pairs).to(dev) if len(w.copy_pairs) else None
-    ps = B.pkv_decode_partition_size(desc, w.num_heads, w.partition_size)
+    ps = B.pkv_decode_partition_size(desc, w.num_seqs, w.num_heads, w.max_context_len,
+                                     w.partition_size)
     ws_bytes = B.pkv_decode_workspace_bytes(desc, w.num_seqs, w.num_heads, w.max_context_len, ps)
     workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
@@ -441,12 +462,11 @@ def run_gpu(args, w, prefill):
     peak, peak_kind = hbm_peak()
     part_mean = sum(part_ms) / len(part_ms) / 1e3
     achieved = dbytes / part_mean / 1e9
-    sha = _sha(os.path.join(ROOT, "paged_kv_cache_130_gb300", "csrc", "decode.cu"))
     tr = NCU_TRAFFIC.get(w.name)
-    traffic = tr["bytes_per_launch"] if tr and tr.get("decode_cu_sha") == sha else None
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == decode_src_sha() else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "decode partition kernel (pkv_paged_attention_partitions)",
+                "kernel": decode_kernel_name(w) + " (pkv_paged_attention_partitions)",
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 

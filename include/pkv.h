@@ -170,10 +170,14 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* caches, int32_t num_layers,
  * Launches: one partition kernel, then (when max_context_len exceeds one
  *   partition) the reduce kernel, chained with programmatic dependent launch.
  * ------------------------------------------------------------------------- */
-/* The partition size a decode with this cache and num_heads query heads uses:
- * `requested` when positive, else the library's choice (about 256 KiB of K+V
- * per KV head and partition, 1 MiB when query heads share KV heads). */
-int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t num_heads,
+/* The partition size a decode of this shape uses: `requested` when positive,
+ * else the library's choice -- one partition per context (no reduce) when
+ * every query head has its own KV head or the cache is FP8, the batch holds at
+ * most 128 sequences, contexts at most 8192 tokens and num_seqs * num_heads is
+ * at least 6x the SM count; otherwise about 256 KiB of K+V per KV head and
+ * partition (1 MiB when a 16-bit cache's KV heads serve groups of 2..16). */
+int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t num_seqs,
+                                  int32_t num_heads, int32_t max_context_len,
                                   int32_t requested);
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,

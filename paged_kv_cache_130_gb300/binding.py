@@ -63,7 +63,7 @@ def load():
         "pkv_status_string": (ctypes.c_char_p, [i32]),
         "pkv_kv_append": (i32, [dp, vp, vp, i32, vp, i64, vp, vp]),
         "pkv_copy_blocks": (i32, [dp, i32, vp, i64, vp, vp]),
-        "pkv_decode_partition_size": (i32, [dp, i32, i32]),
+        "pkv_decode_partition_size": (i32, [dp, i32, i32, i32, i32]),
         "pkv_decode_workspace_bytes": (ctypes.c_size_t, [dp, i32, i32, i32, i32]),
         "pkv_paged_attention_decode": (i32, [dp, vp, i32, i32, i32, vp, i32, vp, i32, f32, i32,
                                              vp, ctypes.c_size_t, vp, vp, vp]),
@@ -162,8 +162,9 @@ def pkv_copy_blocks(caches, block_pairs, dev_err=None, stream=None):
                                   _stream(stream)), "pkv_copy_blocks")
 
 
-def pkv_decode_partition_size(cache, num_heads, requested=0):
-    return int(load().pkv_decode_partition_size(ctypes.byref(cache), int(num_heads),
+def pkv_decode_partition_size(cache, num_seqs, num_heads, max_context_len, requested=0):
+    return int(load().pkv_decode_partition_size(ctypes.byref(cache), int(num_seqs),
+                                                int(num_heads), int(max_context_len),
                                                 int(requested)))
 
 

@@ -1,9 +1,11 @@
-// decode.cu -- paged decode attention, split-context partition kernels.
+// decode.cu -- paged decode attention for grouped query heads (one CTA per
+// work item), and the choice between it and the streaming kernel.
 //
-// One CTA handles one partition (partition_size tokens) of one sequence, for
-// one query head (CUDA-core kernel) or for the whole group of query heads that
-// share a KV head (tensor-core kernel).  Each warp walks a strided subset of
-// the partition's blocks: the physical block id comes from the block table
+// One CTA handles one partition (partition_size tokens) of one sequence for
+// the whole group of query heads that share a KV head.  The grid is ordered
+// longest context first, so the hardware dispatches the largest items first.
+// Each warp walks a strided subset of the partition's blocks: the physical
+// block id comes from the block table
 // (「KV 缓存与分页注意力」 §07 块表), the (block, KV head) tile of K and of V is
 // read with coalesced 16-byte loads straight into registers, and the warp keeps
 // an online softmax (running max and sum, fp32, base 2) with an fp32 P.V
@@ -26,194 +28,33 @@ using dec::locate;
 using dec::PartitionWork;
 
 // =====================================================================
-// CUDA-core kernel: one query head per CTA.
-//
-// Lane layout inside a warp for one (block, KV head) tile of BS x D elements:
-// the tile is BS*D*C bytes = NV 16-byte vectors per lane; vector j of lane l is
-// at byte (j*32 + l)*16, i.e. token j*TPI + l/RV, elements (l%RV)*EPV ... +EPV.
-// Every load instruction covers 512 contiguous bytes.
-// =====================================================================
-template <int CT, int QT, int D, int BS, int NW>
-__global__ void __launch_bounds__(NW * 32, 4) decode_simt_kernel(const DecodeParams p)
-{
-    constexpr int C = Elem<CT>::bytes;
-    constexpr int EPV = 16 / C;          // elements per 16-byte vector
-    constexpr int RV = D / EPV;          // vectors per token row
-    constexpr int TPI = 32 / RV;         // tokens per warp-wide load
-    constexpr int NV = BS / TPI;         // vectors per lane per tile
-    static_assert(RV >= 1 && RV <= 32 && 32 % RV == 0, "row must split evenly over lanes");
-    static_assert(BS % TPI == 0, "block must cover whole warp loads");
-    constexpr int ROWS = 1;
-
-    __shared__ float sm_m[NW * ROWS];
-    __shared__ float sm_l[NW * ROWS];
-    __shared__ __align__(16) float sm_acc[NW * ROWS * D];
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    int64_t idx = blockIdx.x;
-    const int h = (int)(idx % p.num_heads);
-    idx /= p.num_heads;
-    const int s = (int)(idx % p.num_seqs);
-    const int part = (int)(idx / p.num_seqs);
-
-    pdl_launch_dependents();
-
-    const PartitionWork w = locate(p, s, part, threadIdx.x == 0);
-    if (w.idle)
-        return;
-    if (w.zero_out || w.zero_partial) {
-        dec::write_trivial<QT>(p, w, h, 1, threadIdx.x, blockDim.x);
-        return;
-    }
-
-    const int g = h / p.group;
-    const int dchunk = lane % RV;
-    const int tsub = lane / RV;
-
-    // query slice of this lane, pre-multiplied by scale * log2(e) * k_scale
-    float qf[EPV];
-    {
-        const char* qrow = reinterpret_cast<const char*>(p.q) +
-                           (((int64_t)s * p.num_heads + h) * D + dchunk * EPV) * 2;
-#pragma unroll
-        for (int i = 0; i < EPV / 8; ++i) {
-            const uint4 v = ld_ro(qrow + 16 * i);
-            unpack_vec<QT>(v, qf + 8 * i);
-        }
-#pragma unroll
-        for (int e = 0; e < EPV; ++e)
-            qf[e] *= p.qk_scale_log2;
-    }
-
-    const int nblk = ceil_div_i(w.t_end - w.t_begin, BS);
-    const int blk0 = w.t_begin / BS;
-    const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks_per_seq + blk0;
-    const int64_t tile_elems = (int64_t)BS * D;
-    const int64_t head_off = (int64_t)g * tile_elems;
-    const int64_t block_stride = (int64_t)p.num_kv_heads * tile_elems;
-    const char* kbase = reinterpret_cast<const char*>(p.k_cache) + head_off * C;
-    const char* vbase = reinterpret_cast<const char*>(p.v_cache) + head_off * C;
-
-    float m_run = kNegInf;
-    float l_run = 0.f;
-    float acc[EPV];
-#pragma unroll
-    for (int e = 0; e < EPV; ++e)
-        acc[e] = 0.f;
-
-    // this warp's blocks: i = warp, warp + NW, ...; table entries prefetched
-    // 32 at a time into one register per lane
-    for (int chunk = 0; warp + chunk * 32 * NW < nblk; ++chunk) {
-        const int first = warp + chunk * 32 * NW;
-        int my_entry = -1;
-        {
-            const int i = first + lane * NW;
-            if (i < nblk)
-                my_entry = __ldg(table + i);
-        }
-        const int iters = min(32, ceil_div_i(nblk - first, NW));
-        for (int it = 0; it < iters; ++it) {
-            const int i = first + it * NW;
-            const int phys = __shfl_sync(0xffffffffu, my_entry, it);
-            if (phys < 0 || (int64_t)phys >= p.num_blocks) {
-                if (lane == 0)
-                    flag_error(p.dev_err, PKV_DEVERR_BLOCK_ID);
-                continue;
-            }
-            const char* kt = kbase + (int64_t)phys * block_stride * C;
-            const char* vt = vbase + (int64_t)phys * block_stride * C;
-            uint4 kv[NV];
-            uint4 vv[NV];
-#pragma unroll
-            for (int j = 0; j < NV; ++j)
-                kv[j] = ld_stream(kt + (j * 32 + lane) * 16);
-#pragma unroll
-            for (int j = 0; j < NV; ++j)
-                vv[j] = ld_stream(vt + (j * 32 + lane) * 16);
-
-            const int tok0 = w.t_begin + i * BS + tsub;     // token of vector 0
-            float x[NV];
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                float kf[EPV];
-                unpack_vec<CT>(kv[j], kf);
-                float dot = 0.f;
-#pragma unroll
-                for (int e = 0; e < EPV; ++e)
-                    dot = fmaf(qf[e], kf[e], dot);
-#pragma unroll
-                for (int off = RV / 2; off > 0; off >>= 1)
-                    dot += __shfl_xor_sync(0xffffffffu, dot, off);
-                x[j] = (tok0 + j * TPI < w.t_end) ? dot : kNegInf;
-            }
-            float mx = x[0];
-#pragma unroll
-            for (int j = 1; j < NV; ++j)
-                mx = fmaxf(mx, x[j]);
-#pragma unroll
-            for (int off = RV; off < 32; off <<= 1)
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = exp2f(m_run - m_new);
-            m_run = m_new;
-            l_run *= alpha;
-#pragma unroll
-            for (int e = 0; e < EPV; ++e)
-                acc[e] *= alpha;
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                if (tok0 + j * TPI < w.t_end) {
-                    const float pj = exp2f(x[j] - m_new);
-                    l_run += pj;
-                    float vf[EPV];
-                    unpack_vec<CT>(vv[j], vf);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        acc[e] = fmaf(pj, vf[e], acc[e]);
-                }
-            }
-        }
-    }
-
-    // sum over the lanes that share this lane's d-chunk (different tokens)
-#pragma unroll
-    for (int off = RV; off < 32; off <<= 1) {
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e)
-            acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-    }
-    if (lane < RV) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e)
-            sm_acc[warp * D + lane * EPV + e] = acc[e];
-    }
-    if (lane == 0) {
-        sm_m[warp] = m_run;
-        sm_l[warp] = l_run;
-    }
-    __syncthreads();
-    dec::finish_rows<QT, NW, ROWS>(p, w, h, 1, sm_m, sm_l, sm_acc, threadIdx.x, blockDim.x);
-}
-
-// =====================================================================
 // Tensor-core kernel for grouped heads (16-bit caches): one CTA per
 // (sequence, KV head, partition) computes all G <= 16 query heads of the group
 // from one read of each K/V tile, with mma.sync m16n8k16 (fp32 accumulate).
+// Fragments below use g = lane / 4 and t = lane % 4.
 //
-// S = Q K^T per 16-token sub-block: A = Q (rows = heads, padded to 16),
-// B = K^T (8 tokens per n-tile), K-dim = head_dim.  The head_dim index is
-// permuted inside each 32-wide slice so that every fragment register comes
-// from one 16-byte load: thread (r = lane/4, c = lane%4) holds, for k-step
-// 2s'+u, dims 32s' + 8c + 4u + {0,1} and + {2,3}; the same permutation applies
-// to Q and K, which leaves every dot product unchanged.
-// O = P V: A = P straight from the S accumulators (rows = heads, k = tokens),
-// B = V with output column n of n-tile j at dim 64(j/8) + 8n + j%8, so that a
-// thread's B values of one token come from one 16-byte load per 64 dims; the
-// accumulator of thread (r, c) then holds dims 64(j/8) + 16c + {0..15}.
+// Scores are computed transposed, S^T = K Q^T, per 16-token sub-block:
+// A = K (rows = the 16 tokens, k = head_dim), B = Q^T (n = 8 heads of the
+// group per n-tile), so no MMA row is padding when G = 8 or 16.  The head_dim
+// index is permuted inside each 32-wide slice so that every fragment register
+// comes from one 16-byte load: for k-step 2s+u, thread t's k-columns
+// {2t, 2t+1} are dims 32s + 8t + 4u + {0, 1} and {2t+8, 2t+9} are
+// 32s + 8t + 4u + {2, 3}; Q and K share the permutation, so every dot product
+// is unchanged.  The accumulator gives thread (g, t) the scores of tokens g and
+// g + 8 for heads 2t and 2t + 1: the softmax statistics of a head live in the
+// eight lanes with the same t.
+//
+// The output is accumulated transposed too, O^T = V^T P^T: A = V^T (rows =
+// head_dim, k = the 16 tokens), B = P^T.  Row m of m-tile j is dim
+// 64(j/4) + 8(m%8) + 2(j%4) + m/8, so a thread's A values of one token come
+// from one 16-byte load per 64 dims, paired across two tokens with a byte
+// permute.  P^T comes from the score accumulators through movmatrix (an 8x8
+// transpose of 16-bit elements), and the output accumulator of thread (g, t)
+// again belongs to heads 2t and 2t + 1, the heads whose running max it holds.
 // bf16 P is split into a high and a low bf16 part (two MMAs) so that the
 // weights keep ~16 bits; fp16 P is used as is (11 bits, values in [0, 1]).
+// The running max is raised only when some head's block max exceeds it; the
+// rescale is skipped otherwise (its factor would be exactly 1).
 // =====================================================================
 __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1,
                                          bool bf16)
@@ -233,10 +74,13 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
     }
 }
 
-template <int DT>
-__device__ __forceinline__ uint32_t pack_f32x2(float lo, float hi)
+// Transpose of an 8x8 matrix of 16-bit elements held one row pair per lane
+// (lane 4i + j holds row i, columns 2j and 2j + 1).
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x)
 {
-    return pack2(round_to<DT>(lo), round_to<DT>(hi));
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t reg_of(const uint4& v, int i)
@@ -244,16 +88,18 @@ __device__ __forceinline__ uint32_t reg_of(const uint4& v, int i)
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-template <int CT, int D, int BS, int NW, bool TWO_ROWS>
-__global__ void __launch_bounds__(NW * 32, 2) decode_mma_kernel(const DecodeParams p)
+template <int CT, int D, int BS, int NW, int NNT>
+__global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(const DecodeParams p)
 {
     constexpr bool kBf16 = (CT == kBF16);
     constexpr int NS = D / 32;          // 32-wide slices of head_dim (QK k-steps / 2)
     constexpr int NH = D / 64;          // 64-wide halves (V loads per token)
-    constexpr int NT = D / 8;           // n-tiles of the output
+    constexpr int NM = D / 16;          // m-tiles of the transposed output
+    constexpr int SBB = BS / 16;        // 16-token sub-blocks per block
     constexpr int ROWS = 16;
     static_assert(BS % 16 == 0, "tensor-core path needs 16-token sub-blocks");
     static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
+    static_assert(NNT == 1 || NNT == 2, "8 or 16 heads per CTA");
 
     extern __shared__ __align__(16) float smem[];
     float* sm_m = smem;                        // [NW][16]
@@ -262,15 +108,35 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_mma_kernel(const DecodePara
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int r = lane >> 2;
-    const int c = lane & 3;
+    const int gq = lane >> 2;
+    const int t = lane & 3;
     int64_t idx = blockIdx.x;
     const int g = (int)(idx % p.num_kv_heads);
     idx /= p.num_kv_heads;
-    const int s = (int)(idx % p.num_seqs);
+    const int srank = (int)(idx % p.num_seqs);
     const int part = (int)(idx / p.num_seqs);
     const int G = p.group;
     const int head0 = g * G;
+    // grid position -> sequence: longest context first (ties by index) for
+    // batches of up to 128 sequences, in order otherwise
+    int s = srank;
+    if (p.num_seqs <= 128) {
+        __shared__ int sh_ctx[128];
+        __shared__ int sh_seq;
+        for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x)
+            sh_ctx[i] = __ldg(p.context_lens + i);
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
+            const int ci = sh_ctx[i];
+            int rank = 0;
+            for (int j = 0; j < p.num_seqs; ++j)
+                rank += (sh_ctx[j] > ci) || (sh_ctx[j] == ci && j < i);
+            if (rank == srank)
+                sh_seq = i;
+        }
+        __syncthreads();
+        s = sh_seq;
+    }
 
     pdl_launch_dependents();
 
@@ -282,225 +148,253 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_mma_kernel(const DecodePara
         return;
     }
 
-    // Q fragments: rows r and r + 8 of the group (zero past G)
-    uint4 qa[NS];
-    uint4 qb[TWO_ROWS ? NS : 1];
+    // Q^T fragments: head gq (+ 8 for the second n-tile), zero past G
+    uint4 qf[NNT][NS];
     {
         const char* qbase = reinterpret_cast<const char*>(p.q) +
                             ((int64_t)s * p.num_heads + head0) * D * 2;
 #pragma unroll
-        for (int i = 0; i < NS; ++i) {
-            qa[i] = (r < G) ? ld_ro(qbase + ((int64_t)r * D + 32 * i + 8 * c) * 2)
-                            : make_uint4(0, 0, 0, 0);
-            if constexpr (TWO_ROWS)
-                qb[i] = (r + 8 < G) ? ld_ro(qbase + ((int64_t)(r + 8) * D + 32 * i + 8 * c) * 2)
-                                    : make_uint4(0, 0, 0, 0);
-        }
+        for (int n = 0; n < NNT; ++n)
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                const int h = gq + 8 * n;
+                qf[n][i] = (h < G) ? ld_ro(qbase + ((int64_t)h * D + 32 * i + 8 * t) * 2)
+                                   : make_uint4(0, 0, 0, 0);
+            }
     }
 
     const int nblk = ceil_div_i(w.t_end - w.t_begin, BS);
-    const int blk0 = w.t_begin / BS;
-    const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks_per_seq + blk0;
+    const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks_per_seq + w.t_begin / BS;
     const int64_t tile_elems = (int64_t)BS * D;
     const int64_t block_stride = (int64_t)p.num_kv_heads * tile_elems;
     const char* kbase = reinterpret_cast<const char*>(p.k_cache) + (int64_t)g * tile_elems * 2;
     const char* vbase = reinterpret_cast<const char*>(p.v_cache) + (int64_t)g * tile_elems * 2;
     const float qk = p.qk_scale_log2;
 
-    float acc[NT][4];
+    // output accumulators (m-tile j, head tile n) and per-head softmax state
+    // of heads 8n + 2t + {0, 1}
+    float acc[NM][NNT][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
-        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    float m_a = kNegInf, m_b = kNegInf;      // rows r, r + 8
-    float l_a = 0.f, l_b = 0.f;
+    for (int j = 0; j < NM; ++j)
+#pragma unroll
+        for (int n = 0; n < NNT; ++n)
+            acc[j][n][0] = acc[j][n][1] = acc[j][n][2] = acc[j][n][3] = 0.f;
+    float m_h[NNT][2];
+    float l_h[NNT][2];
+#pragma unroll
+    for (int n = 0; n < NNT; ++n)
+        m_h[n][0] = m_h[n][1] = kNegInf, l_h[n][0] = l_h[n][1] = 0.f;
 
-    for (int chunk = 0; warp + chunk * 32 * NW < nblk; ++chunk) {
-        const int first = warp + chunk * 32 * NW;
-        int my_entry = -1;
-        {
-            const int i = first + lane * NW;
-            if (i < nblk)
-                my_entry = __ldg(table + i);
+    // The warp walks blocks warp, warp + NW, ... of the partition, one
+    // 16-token sub-block at a time.  The loop body is unrolled twice, which
+    // lets the compiler issue the next sub-block's loads early.
+    const int my_blocks = nblk > warp ? ceil_div_i(nblk - warp, NW) : 0;
+    const int nsub = my_blocks * SBB;
+    int cur_chunk = -1;
+    int my_entry = -1;
+    auto phys_of = [&](int it) -> int {          // warp-uniform
+        const int ch = it >> 5;
+        if (ch != cur_chunk) {
+            cur_chunk = ch;
+            const int bi = warp + (ch * 32 + lane) * NW;
+            my_entry = bi < nblk ? __ldg(table + bi) : -1;
         }
-        const int iters = min(32, ceil_div_i(nblk - first, NW));
-        for (int it = 0; it < iters; ++it) {
-            const int i = first + it * NW;
-            const int phys = __shfl_sync(0xffffffffu, my_entry, it);
-            if (phys < 0 || (int64_t)phys >= p.num_blocks) {
-                if (lane == 0)
-                    flag_error(p.dev_err, PKV_DEVERR_BLOCK_ID);
-                continue;
+        return __shfl_sync(0xffffffffu, my_entry, it & 31);
+    };
+    // byte offset of sub-block q inside the caches, or -1 for a bad block id
+    auto sub_tile = [&](int q) -> int64_t {
+        const int phys = phys_of(q / SBB);
+        if (phys < 0 || (int64_t)phys >= p.num_blocks) {
+            if (lane == 0 && q % SBB == 0)
+                flag_error(p.dev_err, PKV_DEVERR_BLOCK_ID);
+            return -1;
+        }
+        return ((int64_t)phys * block_stride + (int64_t)(q % SBB) * 16 * D) * 2;
+    };
+    auto load_k = [&](int64_t off, uint4(&k)[2][NS]) {
+        const char* kt = kbase + off;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int i = 0; i < NS; ++i)
+                k[hf][i] = ld_stream(kt + ((hf * 8 + gq) * D + 32 * i + 8 * t) * 2);
+    };
+
+    auto step = [&](int q, int64_t& off, uint4(&kc)[2][NS]) {
+        const int i = warp + (q / SBB) * NW;                  // block of the partition
+        const int tb = w.t_begin + i * BS + (q % SBB) * 16;   // first token of the sub-block
+        const bool live = off >= 0 && tb < w.t_end;           // warp-uniform
+        // V rows of tokens 2t, 2t + 1, 2t + 8, 2t + 9: dims 64 hv + 8 gq + [0, 8)
+        uint4 vc[4][NH];
+        float sc[NNT][4];
+        if (live) {
+            load_k(off, kc);
+            const char* vt = vbase + off;
+#pragma unroll
+            for (int tk = 0; tk < 4; ++tk)
+#pragma unroll
+                for (int hv = 0; hv < NH; ++hv)
+                    vc[tk][hv] = ld_stream(
+                        vt + ((2 * t + (tk & 1) + 8 * (tk >> 1)) * D + 64 * hv + 8 * gq) * 2);
+            // S^T = K Q^T: rows = tokens tb + gq, tb + gq + 8
+#pragma unroll
+            for (int n = 0; n < NNT; ++n)
+                sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+            for (int i2 = 0; i2 < NS; ++i2)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t a[4] = {reg_of(kc[0][i2], 2 * u), reg_of(kc[1][i2], 2 * u),
+                                           reg_of(kc[0][i2], 2 * u + 1),
+                                           reg_of(kc[1][i2], 2 * u + 1)};
+#pragma unroll
+                    for (int n = 0; n < NNT; ++n)
+                        mma16816(sc[n], a, reg_of(qf[n][i2], 2 * u),
+                                 reg_of(qf[n][i2], 2 * u + 1), kBf16);
+                }
+        }
+        const int64_t off_n = q + 1 < nsub ? sub_tile(q + 1) : -1;
+        if (live) {
+            // online softmax (base 2); sc[n][e] is token tb + gq + 8 (e >> 1),
+            // head 8n + 2t + (e & 1)
+            float x[NNT][4];
+            float mn[NNT][2];
+            bool raise = false;
+#pragma unroll
+            for (int n = 0; n < NNT; ++n) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    x[n][e] = (tb + gq + 8 * (e >> 1) < w.t_end) ? sc[n][e] * qk : kNegInf;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float mx = fmaxf(x[n][h], x[n][h + 2]);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    mn[n][h] = fmaxf(m_h[n][h], mx);
+                    raise |= mn[n][h] > m_h[n][h];
+                }
             }
-            const char* kt = kbase + (int64_t)phys * block_stride * 2;
-            const char* vt = vbase + (int64_t)phys * block_stride * 2;
+            if (__any_sync(0xffffffffu, raise)) {
+                float al[NNT][2];
 #pragma unroll
-            for (int sb = 0; sb < BS / 16; ++sb) {
-                const int tb = w.t_begin + i * BS + sb * 16;   // first token of sub-block
-                if (tb >= w.t_end)
-                    break;
-                // loads: K rows (token r, r + 8), V rows (tokens 2c, 2c+1, 2c+8, 2c+9)
-                uint4 kv[2][NS];
-                uint4 vv[4][NH];
+                for (int n = 0; n < NNT; ++n)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                    for (int h = 0; h < 2; ++h) {
+                        al[n][h] = exp2f(m_h[n][h] - mn[n][h]);
+                        m_h[n][h] = mn[n][h];
+                        l_h[n][h] *= al[n][h];
+                    }
 #pragma unroll
-                    for (int i2 = 0; i2 < NS; ++i2)
-                        kv[nt][i2] = ld_stream(kt + ((int64_t)(sb * 16 + nt * 8 + r) * D +
-                                                     32 * i2 + 8 * c) * 2);
+                for (int j = 0; j < NM; ++j)
 #pragma unroll
-                for (int tk = 0; tk < 4; ++tk) {
-                    const int tok = sb * 16 + 2 * c + (tk & 1) + 8 * (tk >> 1);
+                    for (int n = 0; n < NNT; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            acc[j][n][e] *= al[n][e & 1];
+            }
+            float pr[NNT][4];
+#pragma unroll
+            for (int n = 0; n < NNT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    pr[n][e] = x[n][e] == kNegInf ? 0.f : exp2f(x[n][e] - m_h[n][e & 1]);
+                    l_h[n][e & 1] += pr[n][e];
+                }
+
+            // tokens past the context contribute p = 0; clear their V so that
+            // whatever bits sit in those slots cannot make NaN
+#pragma unroll
+            for (int tk = 0; tk < 4; ++tk)
+                if (tb + 2 * t + (tk & 1) + 8 * (tk >> 1) >= w.t_end)
 #pragma unroll
                     for (int hv = 0; hv < NH; ++hv)
-                        vv[tk][hv] = ld_stream(vt + ((int64_t)tok * D + 64 * hv + 8 * r) * 2);
-                }
+                        vc[tk][hv] = make_uint4(0, 0, 0, 0);
 
-                // S = Q K^T for tokens tb + [0, 8) and tb + [8, 16)
-                float sc[2][4];
+            // P^T fragments: rows gq, gq + 8 of the accumulator are tokens, so
+            // the 8x8 transposes give lane (gq, t) head gq, tokens 2t, 2t + 1
+            // (+ 8 for the second register)
+            uint32_t bh[NNT][2];
+            uint32_t bl[NNT][2];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            for (int n = 0; n < NNT; ++n)
 #pragma unroll
-                    for (int i2 = 0; i2 < NS; ++i2) {
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            uint32_t a[4];
-                            a[0] = reg_of(qa[i2], 2 * u);
-                            a[2] = reg_of(qa[i2], 2 * u + 1);
-                            if constexpr (TWO_ROWS) {
-                                a[1] = reg_of(qb[i2], 2 * u);
-                                a[3] = reg_of(qb[i2], 2 * u + 1);
-                            } else {
-                                a[1] = 0u;
-                                a[3] = 0u;
-                            }
-                            mma16816(sc[nt], a, reg_of(kv[nt][i2], 2 * u),
-                                     reg_of(kv[nt][i2], 2 * u + 1), kBf16);
-                        }
-                    }
-                }
-
-                // online softmax (base 2) per row; token of sc[nt][e] is
-                // tb + nt*8 + 2c + (e & 1), row r for e < 2, row r + 8 otherwise
-                float x[2][4];
-                float mx_a = kNegInf, mx_b = kNegInf;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const bool ok = tb + nt * 8 + 2 * c + (e & 1) < w.t_end;
-                        x[nt][e] = ok ? sc[nt][e] * qk : kNegInf;
-                        if (e < 2)
-                            mx_a = fmaxf(mx_a, x[nt][e]);
-                        else
-                            mx_b = fmaxf(mx_b, x[nt][e]);
-                    }
-                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-                const float mn_a = fmaxf(m_a, mx_a);
-                const float mn_b = fmaxf(m_b, mx_b);
-                const float al_a = exp2f(m_a - mn_a);
-                const float al_b = exp2f(m_b - mn_b);
-                m_a = mn_a;
-                m_b = mn_b;
-                l_a *= al_a;
-                l_b *= al_b;
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    acc[j][0] *= al_a;
-                    acc[j][1] *= al_a;
-                    acc[j][2] *= al_b;
-                    acc[j][3] *= al_b;
-                }
-                float pr[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float mref = e < 2 ? mn_a : mn_b;
-                        pr[nt][e] = x[nt][e] == kNegInf ? 0.f : exp2f(x[nt][e] - mref);
-                        if (e < 2)
-                            l_a += pr[nt][e];
-                        else
-                            l_b += pr[nt][e];
-                    }
-
-                // tokens past the context contribute p = 0; clear their V so
-                // that whatever bits sit in the unused slots cannot make NaN
-#pragma unroll
-                for (int tk = 0; tk < 4; ++tk) {
-                    const bool ok = tb + 2 * c + (tk & 1) + 8 * (tk >> 1) < w.t_end;
-                    if (!ok)
-#pragma unroll
-                        for (int hv = 0; hv < NH; ++hv)
-                            vv[tk][hv] = make_uint4(0, 0, 0, 0);
-                }
-
-                // O += P V
-                uint32_t ph[4];
-                uint32_t pl[4];
-                if constexpr (kBf16) {
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        const int nt = q2 >> 1;
-                        const int e0 = (q2 & 1) * 2;
-                        const float v0 = pr[nt][e0], v1 = pr[nt][e0 + 1];
+                for (int hf = 0; hf < 2; ++hf) {
+                    const float v0 = pr[n][2 * hf];
+                    const float v1 = pr[n][2 * hf + 1];
+                    if constexpr (kBf16) {
                         const uint16_t h0 = round_to<kBF16>(v0), h1 = round_to<kBF16>(v1);
                         const float r0 = v0 - __uint_as_float((uint32_t)h0 << 16);
                         const float r1 = v1 - __uint_as_float((uint32_t)h1 << 16);
-                        // fragment order: a0 = row r n-tile 0, a1 = row r+8 n-tile 0,
-                        // a2 = row r n-tile 1, a3 = row r+8 n-tile 1
-                        ph[q2] = pack2(h0, h1);
-                        pl[q2] = pack2(round_to<kBF16>(r0), round_to<kBF16>(r1));
-                    }
-                } else {
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        const int nt = q2 >> 1;
-                        const int e0 = (q2 & 1) * 2;
-                        ph[q2] = pack_f32x2<kF16>(pr[nt][e0], pr[nt][e0 + 1]);
+                        bh[n][hf] = transpose8x8(pack2(h0, h1));
+                        bl[n][hf] =
+                            transpose8x8(pack2(round_to<kBF16>(r0), round_to<kBF16>(r1)));
+                    } else {
+                        bh[n][hf] = transpose8x8(pack2(round_to<kF16>(v0), round_to<kF16>(v1)));
+                        bl[n][hf] = 0u;
                     }
                 }
+
+            // O^T += V^T P^T
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const int hv = j / 8;
-                    const int e = j % 8;
-                    const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-                    const uint32_t b0 = __byte_perm(reg_of(vv[0][hv], e >> 1),
-                                                    reg_of(vv[1][hv], e >> 1), sel);
-                    const uint32_t b1 = __byte_perm(reg_of(vv[2][hv], e >> 1),
-                                                    reg_of(vv[3][hv], e >> 1), sel);
-                    mma16816(acc[j], ph, b0, b1, kBf16);
+            for (int j = 0; j < NM; ++j) {
+                const int hv = j >> 2;
+                const int e = j & 3;
+                const uint32_t lo0 = reg_of(vc[0][hv], e), lo1 = reg_of(vc[1][hv], e);
+                const uint32_t hi0 = reg_of(vc[2][hv], e), hi1 = reg_of(vc[3][hv], e);
+                const uint32_t a[4] = {__byte_perm(lo0, lo1, 0x5410), __byte_perm(lo0, lo1, 0x7632),
+                                       __byte_perm(hi0, hi1, 0x5410), __byte_perm(hi0, hi1, 0x7632)};
+#pragma unroll
+                for (int n = 0; n < NNT; ++n) {
+                    mma16816(acc[j][n], a, bh[n][0], bh[n][1], kBf16);
                     if constexpr (kBf16)
-                        mma16816(acc[j], pl, b0, b1, kBf16);
+                        mma16816(acc[j][n], a, bl[n][0], bl[n][1], kBf16);
                 }
             }
         }
+        off = off_n;
+    };
+
+    uint4 kf[2][NS];
+    int64_t off = nsub > 0 ? sub_tile(0) : -1;
+    for (int q = 0; q < nsub; q += 2) {
+        step(q, off, kf);
+        if (q + 1 < nsub)
+            step(q + 1, off, kf);
     }
 
-    // row sums over the four lanes of a row group
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-    if (c == 0) {
-        sm_m[warp * ROWS + r] = m_a;
-        sm_l[warp * ROWS + r] = l_a;
-        sm_m[warp * ROWS + r + 8] = m_b;
-        sm_l[warp * ROWS + r + 8] = l_b;
-    }
-    // accumulator of n-tile j, element e: row r (+8 for e >= 2),
-    // dim 64*(j/8) + 8*(2c + (e & 1)) + j%8
+    // head sums over the eight lanes of a head
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
+    for (int n = 0; n < NNT; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int row = r + (e >> 1) * 8;
-            const int d = 64 * (j / 8) + 8 * (2 * c + (e & 1)) + (j % 8);
-            sm_acc[(warp * ROWS + row) * D + d] = acc[j][e];
+        for (int h = 0; h < 2; ++h) {
+            float l = l_h[n][h];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            l_h[n][h] = l;
         }
+    if (gq == 0) {
+#pragma unroll
+        for (int n = 0; n < NNT; ++n)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                sm_m[warp * ROWS + 8 * n + 2 * t + h] = m_h[n][h];
+                sm_l[warp * ROWS + 8 * n + 2 * t + h] = l_h[n][h];
+            }
+    }
+    // accumulator (j, n, e): head 8n + 2t + (e & 1),
+    // dim 64 (j / 4) + 8 gq + 2 (j % 4) + (e >> 1)
+#pragma unroll
+    for (int j = 0; j < NM; ++j)
+#pragma unroll
+        for (int n = 0; n < NNT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = 8 * n + 2 * t + (e & 1);
+                const int d = 64 * (j >> 2) + 8 * gq + 2 * (j & 3) + (e >> 1);
+                sm_acc[(warp * ROWS + row) * D + d] = acc[j][n][e];
+            }
     __syncthreads();
     dec::finish_rows<CT, NW, ROWS>(p, w, head0, G, sm_m, sm_l, sm_acc, threadIdx.x,
                                    blockDim.x);
@@ -509,58 +403,22 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_mma_kernel(const DecodePara
 // ------------------------------------------------------------------ dispatch
 
 constexpr int kWarps = 4;
-// The persistent streaming kernel (decode_stream.cu) serves single-head work
-// items; grouped heads use the one-CTA-per-item tensor-core kernel above.
-constexpr bool kUseOneCtaPerItem = false;
 
-template <int CT, int QT, int D, int BS>
-cudaError_t run_simt(const DecodeParams& p, dim3 grid, cudaStream_t stream)
+template <int CT, int D, int BS, int NNT>
+cudaError_t run_mma_heads(const DecodeParams& p, dim3 grid, cudaStream_t stream)
 {
-    decode_simt_kernel<CT, QT, D, BS, kWarps><<<grid, kWarps * 32, 0, stream>>>(p);
+    // merge area: per warp 16 row maxima, 16 row sums and a 16 x D accumulator
+    constexpr size_t smem = sizeof(float) * (2 * kWarps * 16 + kWarps * 16 * D);
+    auto kern = decode_mma_kernel<CT, D, BS, kWarps, NNT>;
+    kern<<<grid, kWarps * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
 template <int CT, int D, int BS>
 cudaError_t run_mma(const DecodeParams& p, dim3 grid, cudaStream_t stream)
 {
-    const size_t smem = sizeof(float) * (2 * kWarps * 16 + kWarps * 16 * D);
-    if (p.group > 8) {
-        auto kern = decode_mma_kernel<CT, D, BS, kWarps, true>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        kern<<<grid, kWarps * 32, smem, stream>>>(p);
-    } else {
-        auto kern = decode_mma_kernel<CT, D, BS, kWarps, false>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        kern<<<grid, kWarps * 32, smem, stream>>>(p);
-    }
-    return cudaGetLastError();
-}
-
-template <int CT, int QT, int D>
-cudaError_t simt_bs(const DecodeParams& p, dim3 grid, cudaStream_t st)
-{
-    switch (p.block_size) {
-    case 8:  return run_simt<CT, QT, D, 8>(p, grid, st);
-    case 16: return run_simt<CT, QT, D, 16>(p, grid, st);
-    case 32: return run_simt<CT, QT, D, 32>(p, grid, st);
-    default: return cudaErrorNotSupported;
-    }
-}
-
-template <int CT, int QT>
-cudaError_t simt_d(const DecodeParams& p, dim3 grid, cudaStream_t st)
-{
-    switch (p.head_dim) {
-    case 64:  return simt_bs<CT, QT, 64>(p, grid, st);
-    case 128: return simt_bs<CT, QT, 128>(p, grid, st);
-    default:  return cudaErrorNotSupported;
-    }
+    return p.group > 8 ? run_mma_heads<CT, D, BS, 2>(p, grid, stream)
+                       : run_mma_heads<CT, D, BS, 1>(p, grid, stream);
 }
 
 template <int CT>
@@ -606,20 +464,12 @@ cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream)
     if (ctas > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)ctas);
-    // one query head per item: the persistent streaming kernel; grouped
-    // heads: the one-CTA-per-item tensor-core kernel below
-    if (!kUseOneCtaPerItem && !mma)
+    // single-head items: the persistent streaming kernel (decode_stream.cu);
+    // grouped heads: the one-CTA-per-item tensor-core kernel above
+    if (!mma)
         return launch_decode_stream(p, false, stream);
-    if (mma) {
-        return p.cache_dtype == kF16 ? mma_shape<kF16>(p, grid, stream)
-                                     : mma_shape<kBF16>(p, grid, stream);
-    }
-    if (p.cache_dtype == kF16)
-        return simt_d<kF16, kF16>(p, grid, stream);
-    if (p.cache_dtype == kBF16)
-        return simt_d<kBF16, kBF16>(p, grid, stream);
-    return p.q_dtype == kF16 ? simt_d<kE4M3, kF16>(p, grid, stream)
-                             : simt_d<kE4M3, kBF16>(p, grid, stream);
+    return p.cache_dtype == kF16 ? mma_shape<kF16>(p, grid, stream)
+                                 : mma_shape<kBF16>(p, grid, stream);
 }
 
 }  // namespace pkv

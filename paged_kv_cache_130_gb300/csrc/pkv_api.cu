@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pkv.h"
 #include "pkv_internal.h"
 
@@ -72,16 +74,41 @@ WorkspaceLayout layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
     return w;
 }
 
-int32_t resolve_partition(const pkv_cache_desc* c, int32_t num_heads, int32_t requested)
+// SM count of the current device, looked up once per device.
+int device_sms()
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 152;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            return 152;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+int32_t resolve_partition(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_heads,
+                          int32_t max_context_len, int32_t requested)
 {
     if (requested > 0)
         return requested;
-    // K+V bytes of one KV head per partition: 256 KiB when every query head
-    // has its own KV head, 1 MiB when a group of query heads shares it (one
-    // work item then serves the whole group)
     const int32_t elem = c->cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
-    const bool grouped = c->num_kv_heads > 0 && num_heads > c->num_kv_heads;
-    const int64_t budget = grouped ? (1 << 20) : (1 << 18);
+    const int32_t group = c->num_kv_heads > 0 ? num_heads / c->num_kv_heads : 1;
+    const bool grouped_items = group >= 2 && group <= 16 && c->cache_dtype != PKV_FP8_E4M3 &&
+                               c->block_size % 16 == 0;
+    if (!grouped_items && num_seqs > 0 && num_seqs <= 128 && max_context_len > 0 &&
+        max_context_len <= 8192 &&
+        (int64_t)num_seqs * num_heads >= 6 * (int64_t)device_sms()) {
+        // one partition per context: the streaming kernel takes the longest
+        // contexts first, which balances this many items without a split
+        return (max_context_len + c->block_size - 1) / c->block_size * c->block_size;
+    }
+    // K+V bytes of one KV head per partition: 256 KiB when a work item serves
+    // one query head, 1 MiB when it serves a group of them
+    const int64_t budget = grouped_items ? (1 << 20) : (1 << 18);
     int32_t tokens = (int32_t)(budget / (2 * c->head_dim * elem));
     tokens = tokens / c->block_size * c->block_size;
     return tokens < c->block_size ? c->block_size : tokens;
@@ -289,12 +316,12 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* caches, int32_t num_layers,
     return PKV_OK;
 }
 
-int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t num_heads,
-                                  int32_t requested)
+int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t num_seqs,
+                                  int32_t num_heads, int32_t max_context_len, int32_t requested)
 {
     if (cache == nullptr || cache->block_size <= 0 || cache->head_dim <= 0)
         return 0;
-    return resolve_partition(cache, num_heads, requested);
+    return resolve_partition(cache, num_seqs, num_heads, max_context_len, requested);
 }
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
@@ -304,7 +331,8 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
     if (cache == nullptr || cache->block_size <= 0 || cache->head_dim <= 0 || num_seqs <= 0 ||
         num_heads <= 0 || max_context_len <= 0 || partition_size < 0)
         return 0;
-    const int32_t part = resolve_partition(cache, num_heads, partition_size);
+    const int32_t part = resolve_partition(cache, num_seqs, num_heads, max_context_len,
+                                           partition_size);
     return (size_t)layout(num_seqs, num_heads, cache->head_dim, max_context_len, part).bytes;
 }
 
@@ -322,7 +350,8 @@ pkv_status pkv_paged_attention_partitions(const pkv_cache_desc* cache, const voi
                                   partition_size, out);
     if (st != PKV_OK || num_seqs == 0)
         return st;
-    const int32_t part = resolve_partition(cache, num_heads, partition_size);
+    const int32_t part = resolve_partition(cache, num_seqs, num_heads, max_context_len,
+                                           partition_size);
     const WorkspaceLayout wl = layout(num_seqs, num_heads, cache->head_dim, max_context_len, part);
     st = check_workspace(wl, workspace, workspace_bytes);
     if (st != PKV_OK)
@@ -367,7 +396,8 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, const void* q
                                   partition_size, out);
     if (st != PKV_OK || num_seqs == 0)
         return st;
-    const int32_t part = resolve_partition(cache, num_heads, partition_size);
+    const int32_t part = resolve_partition(cache, num_seqs, num_heads, max_context_len,
+                                           partition_size);
     const WorkspaceLayout wl = layout(num_seqs, num_heads, cache->head_dim, max_context_len, part);
     st = check_workspace(wl, workspace, workspace_bytes);
     if (st != PKV_OK)

@@ -41,6 +41,37 @@ __device__ __forceinline__ uint4 ld_ro(const void* p)
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
+// 16-byte shared-memory read.
+__device__ __forceinline__ uint4 ld_shared16(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+    return r;
+}
+
+// 16-byte global -> shared asynchronous copy (L2 only), grouped per thread
+// with commit / wait_group: the wait covers this thread's own copies.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gsrc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void st_v4(void* p, uint4 v)
 {
     *reinterpret_cast<uint4*>(p) = v;

@@ -42,11 +42,18 @@ def test_status_strings(lib):
 
 def test_partition_size_and_workspace(lib):
     d = _desc()
-    assert B.pkv_decode_partition_size(d, 8, 0) == 512       # 256 KiB of fp16 K+V
-    assert B.pkv_decode_partition_size(d, 64, 0) == 2048     # grouped heads: 1 MiB
-    assert B.pkv_decode_partition_size(d, 8, 64) == 64
+    # few items: split at 256 KiB of fp16 K+V (512 tokens) per KV head
+    assert B.pkv_decode_partition_size(d, 4, 8, 3000, 0) == 512
+    # grouped heads: 1 MiB (2048 tokens)
+    assert B.pkv_decode_partition_size(d, 64, 64, 3000, 0) == 2048
+    # many single-head items over short contexts: one partition per context
+    d40 = _desc(num_kv_heads=40)
+    assert B.pkv_decode_partition_size(d40, 32, 40, 1398, 0) == 1408
+    assert B.pkv_decode_partition_size(d40, 32, 40, 9000, 0) == 512       # too long
+    assert B.pkv_decode_partition_size(d40, 200, 40, 1398, 0) == 512      # too many to rank
+    assert B.pkv_decode_partition_size(d, 4, 8, 3000, 64) == 64           # as requested
     f8 = _desc(cache_dtype=B.PKV_FP8_E4M3, block_size=32)
-    assert B.pkv_decode_partition_size(f8, 8, 0) == 1024
+    assert B.pkv_decode_partition_size(f8, 4, 8, 30000, 0) == 1024
     # a context within one partition needs no workspace
     assert B.pkv_decode_workspace_bytes(d, 4, 8, 512, 0) == 0
     s, h, p, dim = 3, 8, 2, 128
