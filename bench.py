@@ -42,11 +42,13 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch of the decode partition kernel from an ncu capture,
 # valid while the decode kernel sources hash to "src_sha" (else reported as null)
 NCU_TRAFFIC = {
-    "opt13b_f16": {"bytes_per_launch": 366101760 + 3785728, "src_sha": "dc35b6044e43708b"},
-    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642911232 + 3888640,
-                            "src_sha": "dc35b6044e43708b"},
-    "cow_parallel_sampling_f16": {"bytes_per_launch": 747838208 + 3827200,
-                                  "src_sha": "dc35b6044e43708b"},
+    "opt13b_f16": {"bytes_per_launch": 366103040 + 3534592, "src_sha": "3960089f22385274"},
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642891008 + 3133440,
+                            "src_sha": "3960089f22385274"},
+    # prefix kernel + partition kernel of one shared-prefix decode call
+    "cow_parallel_sampling_f16:shared-prefix": {
+        "bytes_per_launch": 130866944 + 2750464 + 251813888 + 3623680,
+        "src_sha": "3960089f22385274"},
 }
 DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_common.cuh")
 
@@ -57,6 +59,14 @@ def decode_src_sha():
         with open(os.path.join(ROOT, "paged_kv_cache_130_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def shares_prefixes(w):
+    """Whether the shared-prefix kernel takes this workload's shape."""
+    from paged_kv_cache_130_gb300 import workloads as W
+    group = w.num_heads // w.num_kv_heads
+    return (w.cache_dtype == w.io_dtype and w.cache_dtype != W.E4M3 and 1 <= group <= 16
+            and w.block_size in (16, 32) and w.head_dim in (64, 128))
 
 
 def decode_kernel_name(w):
@@ -80,6 +90,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-graphs", action="store_true")
+    ap.add_argument("--shared-prefix", default="auto", choices=["auto", "off"],
+                    help="auto: decode batches with forked sequences through the "
+                         "shared-prefix entry point (each shared block read once per group)")
     ap.add_argument("--flush", default="none", choices=["none", "write"],
                     help="none: the decode inputs alone exceed L2; write: also write "
                          "512 MiB between steps")
@@ -323,13 +336,27 @@ def run_gpu(args, w, prefill):
     pairs = torch.from_numpy(w.copy_pairs).to(dev) if len(w.copy_pairs) else None
     ps = B.pkv_decode_partition_size(desc, w.num_seqs, w.num_heads, w.max_context_len,
                                      w.partition_size)
-    ws_bytes = B.pkv_decode_workspace_bytes(desc, w.num_seqs, w.num_heads, w.max_context_len, ps)
+    grp_begin, grp_blocks = w.prefix_groups()
+    shared = (args.shared_prefix == "auto" and int(grp_blocks.max(initial=0)) > 0
+              and shares_prefixes(w))
+    if shared:
+        gb = torch.from_numpy(grp_begin).to(dev)
+        gp = torch.from_numpy(grp_blocks).to(dev)
+        max_group = int(np.diff(grp_begin).max())
+        max_prefix = int(grp_blocks.max())
+        ws_bytes = B.pkv_shared_prefix_workspace_bytes(desc, w.num_seqs, w.num_heads,
+                                                       w.max_context_len, ps)
+    else:
+        ws_bytes = B.pkv_decode_workspace_bytes(desc, w.num_seqs, w.num_heads,
+                                                w.max_context_len, ps)
     workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
     flush = torch.empty(FLUSH_BYTES if args.flush == "write" else 16, dtype=torch.uint8,
                         device=dev)
     maxp = -(-w.max_context_len // ps)
     launches_per_step = 1 + (1 if pairs is not None else 0) + 1 + (1 if maxp > 1 else 0)
+    if shared:
+        launches_per_step = 1 + (1 if pairs is not None else 0) + 3
 
     def pre():
         if pairs is not None:
@@ -337,12 +364,22 @@ def run_gpu(args, w, prefill):
         B.pkv_kv_append(desc, step_k, step_v, step_slots)
 
     def decode():
-        B.pkv_paged_attention_decode(desc, q, bt, cl, w.max_context_len, w.scale,
-                                     partition_size=ps, workspace=workspace, out=out)
+        if shared:
+            B.pkv_paged_attention_decode_shared_prefix(
+                desc, q, bt, cl, w.max_context_len, gb, gp, max_group, max_prefix, w.scale,
+                partition_size=ps, workspace=workspace, out=out)
+        else:
+            B.pkv_paged_attention_decode(desc, q, bt, cl, w.max_context_len, w.scale,
+                                         partition_size=ps, workspace=workspace, out=out)
 
     def partitions():
-        B.pkv_paged_attention_partitions(desc, q, bt, cl, w.max_context_len, w.scale,
-                                         partition_size=ps, workspace=workspace, out=out)
+        # with shared prefixes the prefix and partition kernels split the
+        # reads between them: the roofline takes the whole decode call
+        if shared:
+            decode()
+        else:
+            B.pkv_paged_attention_partitions(desc, q, bt, cl, w.max_context_len, w.scale,
+                                             partition_size=ps, workspace=workspace, out=out)
 
     def maybe_flush(i):
         if args.flush == "write":
@@ -431,6 +468,10 @@ def run_gpu(args, w, prefill):
         h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
         if h_pairs is not None:
             h2d += h_pairs.numel() * 8
+        if shared:
+            h_gb = torch.from_numpy(grp_begin).pin_memory()
+            h_gp = torch.from_numpy(grp_blocks).pin_memory()
+            h2d += 4 * (h_gb.numel() + h_gp.numel())
         d2h = h_out.numel() * h_out.element_size()
         e2e_ms = []
         for i in range(args.steps + args.warmup):
@@ -446,6 +487,9 @@ def run_gpu(args, w, prefill):
             cl.copy_(h_cl, non_blocking=True)
             if h_pairs is not None:
                 pairs.copy_(h_pairs, non_blocking=True)
+            if shared:
+                gb.copy_(h_gb, non_blocking=True)
+                gp.copy_(h_gp, non_blocking=True)
             pre()
             decode()
             h_out.copy_(out, non_blocking=True)
@@ -461,12 +505,19 @@ def run_gpu(args, w, prefill):
 
     peak, peak_kind = hbm_peak()
     part_mean = sum(part_ms) / len(part_ms) / 1e3
-    achieved = dbytes / part_mean / 1e9
-    tr = NCU_TRAFFIC.get(w.name)
+    # bytes the timed kernel must move: with shared prefixes every distinct
+    # block once (the prefix kernel reads a shared block once per group)
+    rbytes = dbytes - w.kv_bytes() + w.unique_kv_bytes() if shared else dbytes
+    achieved = rbytes / part_mean / 1e9
+    tr = NCU_TRAFFIC.get(w.name + (":shared-prefix" if shared else ""))
     traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == decode_src_sha() else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": decode_kernel_name(w) + " (pkv_paged_attention_partitions)",
+                "kernel": ("shared-prefix decode call: decode_mma_kernel over the prefixes, "
+                           + decode_kernel_name(w) + " over the rest, lse_reduce_kernel"
+                           if shared else
+                           decode_kernel_name(w) + " (pkv_paged_attention_partitions)"),
+                "algorithmic_bytes": rbytes,
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
@@ -477,6 +528,8 @@ def run_gpu(args, w, prefill):
     cfg["timing"] = "CUDA events around CUDA-graph replays" if not args.no_graphs \
         else "CUDA events around direct calls"
     cfg["partition_size"] = ps
+    cfg["shared_prefix"] = ({"groups": int(len(grp_blocks)), "max_group": max_group,
+                             "prefix_blocks": max_prefix} if shared else None)
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3 / args.steps, "higher_is_better": True,

@@ -79,6 +79,8 @@ typedef enum pkv_dtype {
 #define PKV_DEVERR_COPY_PAIR 8   /* copy pair entry outside [0, num_blocks)    */
 #define PKV_DEVERR_TIMEOUT   16  /* a kernel's bounded wait on its own copies  */
                                  /* ran out; that call's output is not valid   */
+#define PKV_DEVERR_PREFIX    32  /* a shared-prefix group entry is unusable, or */
+                                 /* a member's table differs within the prefix */
 
 /* One layer's cache.  k_cache / v_cache: device, caller-owned, layout above.
  * k_scale / v_scale: for an FP8 cache, the stored code times the scale is the
@@ -171,11 +173,13 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* caches, int32_t num_layers,
  *   partition) the reduce kernel, chained with programmatic dependent launch.
  * ------------------------------------------------------------------------- */
 /* The partition size a decode of this shape uses: `requested` when positive,
- * else the library's choice -- one partition per context (no reduce) when
- * every query head has its own KV head or the cache is FP8, the batch holds at
- * most 128 sequences, contexts at most 8192 tokens and num_seqs * num_heads is
- * at least 6x the SM count; otherwise about 256 KiB of K+V per KV head and
- * partition (1 MiB when a 16-bit cache's KV heads serve groups of 2..16). */
+ * else the library's choice -- one partition per context (no reduce) when the
+ * batch holds at most 128 sequences, contexts at most 8192 tokens and there
+ * are enough work items: num_seqs * num_heads >= 6x the SM count when every
+ * query head has its own KV head or the cache is FP8, num_seqs * num_kv_heads
+ * >= 3x the SM count when a 16-bit cache's KV heads serve groups of 2..16;
+ * otherwise about 256 KiB of K+V per KV head and partition (1 MiB for the
+ * grouped case). */
 int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t num_seqs,
                                   int32_t num_heads, int32_t max_context_len,
                                   int32_t requested);
@@ -225,6 +229,62 @@ pkv_status pkv_lse_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
                           int32_t partition_size, const void* workspace,
                           size_t workspace_bytes, int32_t out_dtype, void* out,
                           pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Shared-prefix decode -- the decode above for a batch in which groups of
+ * sequences share their leading blocks, as forked sequences do (parallel
+ * sampling and beam search share the prompt's blocks by reference count:
+ * 「KV 缓存与分页注意力」 §08 写时复制).  The result is the attention defined
+ * above; only the reads change: a shared block is read once per group, KV head
+ * and 8 or 16 query rows (members x query heads of the KV head) instead of
+ * once per member and query head.
+ *
+ * Attention over [0, c) splits exactly at the end P of the shared prefix: the
+ * prefix kernel writes (m, l, o) partials of [0, P) for every member and head,
+ * the partition kernel those of [P, c), and the log-sum-exp reduce merges them.
+ *
+ * Groups: sequences [group_begin[i], group_begin[i + 1]) form group i.
+ * group_begin          device int32 [num_groups + 1], ascending, starting at 0
+ *                      and ending at num_seqs; every sequence is in one group
+ *                      (a sequence that shares nothing is a group of one with
+ *                      no prefix).
+ * group_prefix_blocks  device int32 [num_groups]: P_i / block_size, the number
+ *                      of leading block-table entries that every member of
+ *                      group i holds equal to its first member's (0: nothing
+ *                      shared).  Each member's context must hold at least
+ *                      P_i tokens.
+ * max_group_size, max_prefix_blocks  host upper bounds that size the prefix
+ *                      kernel's grid, like max_context_len;
+ *                      max_prefix_blocks * block_size <= max_context_len and
+ *                      max_prefix_blocks <= max_blocks_per_seq.
+ * workspace            at least pkv_shared_prefix_workspace_bytes(...) bytes
+ *                      (the decode layout above with four more partials per
+ *                      row: a shared prefix of P tokens is cut into at most
+ *                      four partitions of round_up(ceil(max_prefix_blocks *
+ *                      block_size / 4), block_size) tokens, which come before
+ *                      the partitions of the rest of the context).
+ * Device checks (with dev_err): a group entry out of range or a prefix above
+ * max_prefix_blocks flags PKV_DEVERR_PREFIX and that group's prefix is not
+ * computed; a member past max_group_size or with a context shorter than its
+ * prefix flags PKV_DEVERR_CONTEXT and its output is zero; a member whose table
+ * differs from the first member's inside the prefix flags PKV_DEVERR_PREFIX
+ * (its output then uses the first member's blocks).
+ * Supported: F16 or BF16 caches with q of the same type, 1..16 query heads per
+ * KV head; anything else returns PKV_ERR_UNSUPPORTED and launches nothing.
+ * num_groups == 0 or max_prefix_blocks == 0 gives the plain decode.
+ * Launches: prefix kernel, partition kernel, reduce.
+ * ------------------------------------------------------------------------- */
+size_t pkv_shared_prefix_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
+                                         int32_t num_heads, int32_t max_context_len,
+                                         int32_t partition_size);
+
+pkv_status pkv_paged_attention_decode_shared_prefix(
+    const pkv_cache_desc* cache, const void* q, int32_t q_dtype, int32_t num_seqs,
+    int32_t num_heads, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t max_context_len, int32_t num_groups,
+    const int32_t* group_begin, const int32_t* group_prefix_blocks, int32_t max_group_size,
+    int32_t max_prefix_blocks, float scale, int32_t partition_size, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* out, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * pkv_paged_attention_decode_static_ws -- the decode above for callers that

@@ -25,6 +25,7 @@ PKV_ERR_SCRATCH_LIMIT = 5
 PKV_STATIC_SCRATCH_BYTES = 32 << 20
 PKV_DEVERR_SLOT, PKV_DEVERR_BLOCK_ID, PKV_DEVERR_CONTEXT, PKV_DEVERR_COPY_PAIR = 1, 2, 4, 8
 PKV_DEVERR_TIMEOUT = 16
+PKV_DEVERR_PREFIX = 32
 
 
 class PkvError(RuntimeError):
@@ -72,6 +73,10 @@ def load():
         "pkv_lse_reduce": (i32, [i32, i32, i32, vp, i32, i32, vp, ctypes.c_size_t, i32, vp, vp]),
         "pkv_paged_attention_decode_static_ws": (i32, [dp, vp, i32, i32, i32, vp, i32, vp, i32,
                                                        f32, i32, vp, vp, vp]),
+        "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [dp, i32, i32, i32, i32]),
+        "pkv_paged_attention_decode_shared_prefix": (i32, [dp, vp, i32, i32, i32, vp, i32, vp,
+                                                           i32, i32, vp, vp, i32, i32, f32, i32,
+                                                           vp, ctypes.c_size_t, vp, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -243,3 +248,47 @@ def pkv_paged_attention_decode_static_ws(cache, q, block_tables, context_lens, m
         int(partition_size), _ptr(dev_err), _ptr(out), _stream(stream)),
         "pkv_paged_attention_decode_static_ws")
     return out
+
+
+def pkv_shared_prefix_workspace_bytes(cache, num_seqs, num_heads, max_context_len,
+                                      partition_size=0):
+    return int(load().pkv_shared_prefix_workspace_bytes(ctypes.byref(cache), num_seqs,
+                                                        num_heads, max_context_len,
+                                                        partition_size))
+
+
+def pkv_paged_attention_decode_shared_prefix(cache, q, block_tables, context_lens,
+                                             max_context_len, group_begin, group_prefix_blocks,
+                                             max_group_size, max_prefix_blocks, scale,
+                                             partition_size=0, workspace=None, dev_err=None,
+                                             out=None, stream=None):
+    """Decode where the sequences [group_begin[i], group_begin[i+1]) share their
+    first group_prefix_blocks[i] blocks (int32 device tensors); the two
+    max_* arguments are host upper bounds."""
+    _dense(q, "q")
+    _dense(block_tables, "block_tables")
+    _dense(context_lens, "context_lens")
+    _dense(group_begin, "group_begin")
+    _dense(group_prefix_blocks, "group_prefix_blocks")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                    (group_begin, "group_begin"), (group_prefix_blocks, "group_prefix_blocks")):
+        if t.dtype != torch.int32:
+            raise ValueError("%s must be int32" % name)
+    num_groups = group_prefix_blocks.numel()
+    if group_begin.numel() != num_groups + 1:
+        raise ValueError("group_begin needs num_groups + 1 entries")
+    s, h, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    need = pkv_shared_prefix_workspace_bytes(cache, s, h, max_context_len, partition_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pkv_paged_attention_decode_shared_prefix(
+        ctypes.byref(cache), _ptr(q), dtype_code(q.dtype), s, h, _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), num_groups,
+        _ptr(group_begin), _ptr(group_prefix_blocks), int(max_group_size),
+        int(max_prefix_blocks), float(scale), int(partition_size), _ptr(workspace), ws_bytes,
+        _ptr(dev_err), _ptr(out), _stream(stream)), "pkv_paged_attention_decode_shared_prefix")
+    return out
+

@@ -159,3 +159,42 @@ class BlockManager:
                 raise ValueError("sequence holds more blocks than max_blocks")
             out[i, :len(s.table)] = s.table
         return out
+
+
+def shared_prefix_groups(block_tables, context_lens, block_size):
+    """Groups of consecutive sequences that share their leading blocks.
+
+    Forked sequences hold the same physical blocks for the prompt they share
+    (「KV 缓存与分页注意力」 §08 共用，写时复制): their block-table rows start
+    with equal entries.  A group extends over the following rows while their
+    first entry equals the group's first row's; its prefix is the number of
+    leading entries every member holds equal to the first row's, counting only
+    blocks that are full in every member (so that prefix * block_size tokens
+    lie inside each member's context).
+
+    Returns ``(group_begin, prefix_blocks)``: int32 arrays of ``num_groups + 1``
+    and ``num_groups`` entries; rows [group_begin[i], group_begin[i + 1]) form
+    group i.  A row that shares nothing is a group of one with prefix 0.
+    """
+    tables = np.asarray(block_tables)
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    n = len(ctx)
+    begin, prefix = [0], []
+    i = 0
+    while i < n:
+        common = int(ctx[i] // block_size)
+        j = i + 1
+        while j < n and common > 0:
+            full = int(ctx[j] // block_size)
+            k = 0
+            lim = min(common, full)
+            while k < lim and tables[j, k] == tables[i, k]:
+                k += 1
+            if k == 0:
+                break
+            common = k
+            j += 1
+        prefix.append(common if j - i >= 2 else 0)
+        begin.append(j)
+        i = j
+    return np.array(begin, dtype=np.int32), np.array(prefix, dtype=np.int32)

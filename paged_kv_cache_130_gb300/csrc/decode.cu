@@ -88,7 +88,7 @@ __device__ __forceinline__ uint32_t reg_of(const uint4& v, int i)
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-template <int CT, int D, int BS, int NW, int NNT>
+template <int CT, int D, int BS, int NW, int NNT, bool PREFIX>
 __global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(const DecodeParams p)
 {
     constexpr bool kBf16 = (CT == kBF16);
@@ -110,61 +110,130 @@ __global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(c
     const int warp = threadIdx.x >> 5;
     const int gq = lane >> 2;
     const int t = lane & 3;
+    constexpr int RT = 8 * NNT;                    // rows of one CTA
+    const int G = p.group;
     int64_t idx = blockIdx.x;
     const int g = (int)(idx % p.num_kv_heads);
     idx /= p.num_kv_heads;
-    const int srank = (int)(idx % p.num_seqs);
-    const int part = (int)(idx / p.num_seqs);
-    const int G = p.group;
-    const int head0 = g * G;
-    // grid position -> sequence: longest context first (ties by index) for
-    // batches of up to 128 sequences, in order otherwise
-    int s = srank;
-    if (p.num_seqs <= 128) {
-        __shared__ int sh_ctx[128];
-        __shared__ int sh_seq;
-        for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x)
-            sh_ctx[i] = __ldg(p.context_lens + i);
-        __syncthreads();
-        for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
-            const int ci = sh_ctx[i];
-            int rank = 0;
-            for (int j = 0; j < p.num_seqs; ++j)
-                rank += (sh_ctx[j] > ci) || (sh_ctx[j] == ci && j < i);
-            if (rank == srank)
-                sh_seq = i;
+
+    // The CTA's rows (query vectors), token range [t_begin, t_end) and block
+    // table.  Decode: the G query heads of KV head g of one sequence, over one
+    // partition of its context after any shared prefix.  Prefix: rows
+    // row0 + [0, RT) of the group's members x G heads, over one partition of
+    // the group's shared prefix, read through the first member's table.
+    int s = 0;                 // decode: the sequence
+    int b0 = 0;                // prefix: the group's first sequence
+    int row0 = 0;
+    int nrows = G;
+    int t_begin = 0;
+    int t_end = 0;
+    int slot = 0;
+    bool direct = false;
+    const int32_t* table = nullptr;
+    if constexpr (PREFIX) {
+        const int ntiles = ceil_div_i(p.max_group_size * G, RT);
+        const int tile = (int)(idx % ntiles);
+        idx /= ntiles;
+        const int grp = (int)(idx % p.num_groups);
+        const int chunk = (int)(idx / p.num_groups);
+        b0 = __ldg(p.grp_begin + grp);
+        const int b1 = __ldg(p.grp_begin + grp + 1);
+        const int blocks = __ldg(p.grp_prefix_blocks + grp);
+        const bool first = g == 0 && tile == 0 && chunk == 0 && threadIdx.x == 0;
+        if (b0 < 0 || b1 < b0 || b1 > p.num_seqs || blocks < 0 ||
+            blocks > min(p.max_prefix_blocks, p.max_blocks_per_seq)) {
+            if (first)
+                flag_error(p.dev_err, PKV_DEVERR_PREFIX);
+            return;
         }
-        __syncthreads();
-        s = sh_seq;
-    }
-
-    pdl_launch_dependents();
-
-    const PartitionWork w = locate(p, s, part, threadIdx.x == 0);
-    if (w.idle)
-        return;
-    if (w.zero_out || w.zero_partial) {
-        dec::write_trivial<CT>(p, w, head0, G, threadIdx.x, blockDim.x);
-        return;
-    }
-
-    // Q^T fragments: head gq (+ 8 for the second n-tile), zero past G
-    uint4 qf[NNT][NS];
-    {
-        const char* qbase = reinterpret_cast<const char*>(p.q) +
-                            ((int64_t)s * p.num_heads + head0) * D * 2;
-#pragma unroll
-        for (int n = 0; n < NNT; ++n)
-#pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                const int h = gq + 8 * n;
-                qf[n][i] = (h < G) ? ld_ro(qbase + ((int64_t)h * D + 32 * i + 8 * t) * 2)
-                                   : make_uint4(0, 0, 0, 0);
+        const int nmem = min(b1 - b0, p.max_group_size);
+        // every member's table must hold the first member's prefix blocks
+        if (g == 0 && tile == 0 && chunk == 0) {
+            const int32_t* lead = p.block_tables + (int64_t)b0 * p.max_blocks_per_seq;
+            for (int i = threadIdx.x; i < (nmem - 1) * blocks; i += blockDim.x) {
+                const int m = 1 + i / blocks;
+                const int b = i % blocks;
+                if (__ldg(lead + (int64_t)m * p.max_blocks_per_seq + b) != __ldg(lead + b))
+                    flag_error(p.dev_err, PKV_DEVERR_PREFIX);
             }
-    }
+        }
+        t_begin = chunk * p.prefix_partition;
+        t_end = min(blocks * BS, t_begin + p.prefix_partition);
+        row0 = tile * RT;
+        nrows = min(RT, nmem * G - row0);
+        if (t_begin >= t_end || nrows <= 0)
+            return;
+        slot = chunk;
+        table = p.block_tables + (int64_t)b0 * p.max_blocks_per_seq + t_begin / BS;
+        pdl_launch_dependents();
+    } else {
+        const int srank = (int)(idx % p.num_seqs);
+        const int part = (int)(idx / p.num_seqs);
+        // grid position -> sequence: longest context first (ties by index)
+        // for batches of up to 128 sequences, in order otherwise
+        s = srank;
+        if (p.num_seqs <= 128) {
+            __shared__ int sh_ctx[128];
+            __shared__ int sh_seq;
+            for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x)
+                sh_ctx[i] = __ldg(p.context_lens + i);
+            __syncthreads();
+            for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
+                const int ci = sh_ctx[i];
+                int rank = 0;
+                for (int j = 0; j < p.num_seqs; ++j)
+                    rank += (sh_ctx[j] > ci) || (sh_ctx[j] == ci && j < i);
+                if (rank == srank)
+                    sh_seq = i;
+            }
+            __syncthreads();
+            s = sh_seq;
+        }
 
-    const int nblk = ceil_div_i(w.t_end - w.t_begin, BS);
-    const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks_per_seq + w.t_begin / BS;
+        pdl_launch_dependents();
+
+        const PartitionWork w = locate(p, s, part, threadIdx.x == 0);
+        if (w.idle || w.zero_out || w.zero_partial) {
+            if (!w.idle)
+                dec::write_trivial<CT>(p, w, g * G, G, threadIdx.x, blockDim.x);
+            if (p.wait_prior && threadIdx.x == 0)
+                pdl_wait_primary();
+            return;
+        }
+        t_begin = w.t_begin;
+        t_end = w.t_end;
+        table = p.block_tables + (int64_t)s * p.max_blocks_per_seq + t_begin / BS;
+    }
+    // row r -> (sequence, query head)
+    auto row_of = [&](int r) -> int2 {
+        if constexpr (PREFIX) {
+            const int rho = row0 + r;
+            return make_int2(b0 + rho / G, g * G + rho % G);
+        } else {
+            return make_int2(s, g * G + r);
+        }
+    };
+
+    // Q^T fragments: rows gq (+ 8 for the second n-tile), zero past nrows
+    // kept in shared memory as sq[n][i][lane] (each lane reads back its own
+    // 16 bytes: conflict-free) rather than in registers, which the K/V loads
+    // of the block loop need
+    uint4* sq = reinterpret_cast<uint4*>(sm_acc + NW * ROWS * D);     // [NNT][NS][32]
+    for (int i = threadIdx.x; i < NNT * NS * 32; i += blockDim.x) {
+        const int ln = i & 31;
+        const int r = (ln >> 2) + 8 * (i / (NS * 32));
+        const int sl = (i >> 5) % NS;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < nrows) {
+            const int2 sh = row_of(r);
+            v = ld_ro(reinterpret_cast<const char*>(p.q) +
+                      (((int64_t)sh.x * p.num_heads + sh.y) * D + 32 * sl + 8 * (ln & 3)) * 2);
+        }
+        sq[i] = v;
+    }
+    __syncthreads();
+
+    const int nblk = ceil_div_i(t_end - t_begin, BS);
     const int64_t tile_elems = (int64_t)BS * D;
     const int64_t block_stride = (int64_t)p.num_kv_heads * tile_elems;
     const char* kbase = reinterpret_cast<const char*>(p.k_cache) + (int64_t)g * tile_elems * 2;
@@ -222,8 +291,8 @@ __global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(c
 
     auto step = [&](int q, int64_t& off, uint4(&kc)[2][NS]) {
         const int i = warp + (q / SBB) * NW;                  // block of the partition
-        const int tb = w.t_begin + i * BS + (q % SBB) * 16;   // first token of the sub-block
-        const bool live = off >= 0 && tb < w.t_end;           // warp-uniform
+        const int tb = t_begin + i * BS + (q % SBB) * 16;   // first token of the sub-block
+        const bool live = off >= 0 && tb < t_end;           // warp-uniform
         // V rows of tokens 2t, 2t + 1, 2t + 8, 2t + 9: dims 64 hv + 8 gq + [0, 8)
         uint4 vc[4][NH];
         float sc[NNT][4];
@@ -241,7 +310,11 @@ __global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(c
             for (int n = 0; n < NNT; ++n)
                 sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
-            for (int i2 = 0; i2 < NS; ++i2)
+            for (int i2 = 0; i2 < NS; ++i2) {
+                uint4 qv[NNT];
+#pragma unroll
+                for (int n = 0; n < NNT; ++n)
+                    qv[n] = ld_shared16(sq + (n * NS + i2) * 32 + lane);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const uint32_t a[4] = {reg_of(kc[0][i2], 2 * u), reg_of(kc[1][i2], 2 * u),
@@ -249,9 +322,10 @@ __global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(c
                                            reg_of(kc[1][i2], 2 * u + 1)};
 #pragma unroll
                     for (int n = 0; n < NNT; ++n)
-                        mma16816(sc[n], a, reg_of(qf[n][i2], 2 * u),
-                                 reg_of(qf[n][i2], 2 * u + 1), kBf16);
+                        mma16816(sc[n], a, reg_of(qv[n], 2 * u), reg_of(qv[n], 2 * u + 1),
+                                 kBf16);
                 }
+            }
         }
         const int64_t off_n = q + 1 < nsub ? sub_tile(q + 1) : -1;
         if (live) {
@@ -264,7 +338,7 @@ __global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(c
             for (int n = 0; n < NNT; ++n) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    x[n][e] = (tb + gq + 8 * (e >> 1) < w.t_end) ? sc[n][e] * qk : kNegInf;
+                    x[n][e] = (tb + gq + 8 * (e >> 1) < t_end) ? sc[n][e] * qk : kNegInf;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float mx = fmaxf(x[n][h], x[n][h + 2]);
@@ -306,7 +380,7 @@ __global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(c
             // whatever bits sit in those slots cannot make NaN
 #pragma unroll
             for (int tk = 0; tk < 4; ++tk)
-                if (tb + 2 * t + (tk & 1) + 8 * (tk >> 1) >= w.t_end)
+                if (tb + 2 * t + (tk & 1) + 8 * (tk >> 1) >= t_end)
 #pragma unroll
                     for (int hv = 0; hv < NH; ++hv)
                         vc[tk][hv] = make_uint4(0, 0, 0, 0);
@@ -395,39 +469,60 @@ __global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(c
                 const int d = 64 * (j >> 2) + 8 * gq + 2 * (j & 3) + (e >> 1);
                 sm_acc[(warp * ROWS + row) * D + d] = acc[j][n][e];
             }
+    if constexpr (!PREFIX) {
+        // where this item's result goes (recomputed: nothing stays live
+        // across the loop for it)
+        const PartitionWork w = locate(p, s, (int)(blockIdx.x / p.num_kv_heads / p.num_seqs),
+                                       false);
+        slot = w.slot;
+        direct = w.direct;
+    }
     __syncthreads();
-    dec::finish_rows<CT, NW, ROWS>(p, w, head0, G, sm_m, sm_l, sm_acc, threadIdx.x,
-                                   blockDim.x);
+    dec::finish_rows_map<CT, NW, ROWS>(p, direct, slot, nrows, row_of, sm_m, sm_l, sm_acc,
+                                       threadIdx.x, blockDim.x);
+    if (!PREFIX && p.wait_prior && threadIdx.x == 0)
+        pdl_wait_primary();
 }
 
 // ------------------------------------------------------------------ dispatch
 
 constexpr int kWarps = 4;
 
-template <int CT, int D, int BS, int NNT>
+template <int CT, int D, int BS, int NNT, bool PREFIX>
 cudaError_t run_mma_heads(const DecodeParams& p, dim3 grid, cudaStream_t stream)
 {
-    // merge area: per warp 16 row maxima, 16 row sums and a 16 x D accumulator
-    constexpr size_t smem = sizeof(float) * (2 * kWarps * 16 + kWarps * 16 * D);
-    auto kern = decode_mma_kernel<CT, D, BS, kWarps, NNT>;
-    kern<<<grid, kWarps * 32, smem, stream>>>(p);
-    return cudaGetLastError();
+    // merge area (per warp 16 row maxima, 16 row sums and a 16 x D
+    // accumulator), then the Q fragments (NNT x D/32 x 32 lanes x 16 bytes)
+    constexpr size_t smem = sizeof(float) * (2 * kWarps * 16 + kWarps * 16 * D) + NNT * D * 16;
+    auto kern = decode_mma_kernel<CT, D, BS, kWarps, NNT, PREFIX>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (!PREFIX && p.wait_prior) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int CT, int D, int BS>
-cudaError_t run_mma(const DecodeParams& p, dim3 grid, cudaStream_t stream)
+// rows per CTA: 8 when they fit, else 16
+template <int CT, int D, int BS, bool PREFIX>
+cudaError_t run_mma(const DecodeParams& p, int rows, dim3 grid, cudaStream_t stream)
 {
-    return p.group > 8 ? run_mma_heads<CT, D, BS, 2>(p, grid, stream)
-                       : run_mma_heads<CT, D, BS, 1>(p, grid, stream);
+    return rows > 8 ? run_mma_heads<CT, D, BS, 2, PREFIX>(p, grid, stream)
+                    : run_mma_heads<CT, D, BS, 1, PREFIX>(p, grid, stream);
 }
 
-template <int CT>
-cudaError_t mma_shape(const DecodeParams& p, dim3 grid, cudaStream_t st)
+template <int CT, bool PREFIX>
+cudaError_t mma_shape(const DecodeParams& p, int rows, dim3 grid, cudaStream_t st)
 {
-    if (p.head_dim == 64 && p.block_size == 16) return run_mma<CT, 64, 16>(p, grid, st);
-    if (p.head_dim == 64 && p.block_size == 32) return run_mma<CT, 64, 32>(p, grid, st);
-    if (p.head_dim == 128 && p.block_size == 16) return run_mma<CT, 128, 16>(p, grid, st);
-    if (p.head_dim == 128 && p.block_size == 32) return run_mma<CT, 128, 32>(p, grid, st);
+    if (p.head_dim == 64 && p.block_size == 16) return run_mma<CT, 64, 16, PREFIX>(p, rows, grid, st);
+    if (p.head_dim == 64 && p.block_size == 32) return run_mma<CT, 64, 32, PREFIX>(p, rows, grid, st);
+    if (p.head_dim == 128 && p.block_size == 16) return run_mma<CT, 128, 16, PREFIX>(p, rows, grid, st);
+    if (p.head_dim == 128 && p.block_size == 32) return run_mma<CT, 128, 32, PREFIX>(p, rows, grid, st);
     return cudaErrorNotSupported;
 }
 
@@ -458,7 +553,7 @@ cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream)
         return cudaErrorNotSupported;
     const bool mma = use_mma(p);
     const int64_t heads = mma ? p.num_kv_heads : p.num_heads;
-    const int64_t ctas = (int64_t)p.max_partitions * p.num_seqs * heads;
+    const int64_t ctas = (int64_t)p.grid_partitions * p.num_seqs * heads;
     if (ctas <= 0)
         return cudaSuccess;
     if (ctas > 0x7fffffffLL)
@@ -468,8 +563,40 @@ cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream)
     // grouped heads: the one-CTA-per-item tensor-core kernel above
     if (!mma)
         return launch_decode_stream(p, false, stream);
-    return p.cache_dtype == kF16 ? mma_shape<kF16>(p, grid, stream)
-                                 : mma_shape<kBF16>(p, grid, stream);
+    return p.cache_dtype == kF16 ? mma_shape<kF16, false>(p, p.group, grid, stream)
+                                 : mma_shape<kBF16, false>(p, p.group, grid, stream);
+}
+
+bool prefix_kernel_supported(int cache_dtype, int q_dtype, int head_dim, int block_size,
+                             int group)
+{
+    return (head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32) &&
+           (cache_dtype == kF16 || cache_dtype == kBF16) && cache_dtype == q_dtype &&
+           group >= 1 && group <= 16;
+}
+
+cudaError_t launch_decode_prefix(const DecodeParams& p, cudaStream_t stream)
+{
+    if (!prefix_kernel_supported(p.cache_dtype, p.q_dtype, p.head_dim, p.block_size, p.group))
+        return cudaErrorNotSupported;
+    if (p.grp_begin == nullptr || p.num_groups <= 0 || p.max_group_size <= 0 ||
+        p.max_prefix_blocks <= 0)
+        return cudaSuccess;
+    // members x heads of a KV head, in tiles of 8 or 16 rows
+    const int64_t rows = (int64_t)p.max_group_size * p.group;
+    const int rt = rows > 8 ? 16 : 8;
+    const int64_t tiles = (rows + rt - 1) / rt;
+    if (p.prefix_partition <= 0)
+        return cudaErrorInvalidValue;
+    const int64_t chunks = ((int64_t)p.max_prefix_blocks * p.block_size + p.prefix_partition - 1) /
+                           p.prefix_partition;
+    const int64_t ctas = chunks * p.num_groups * tiles * p.num_kv_heads;
+    if (ctas > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)ctas);
+    const int r = (int)(rows > 8 ? 16 : 8);
+    return p.cache_dtype == kF16 ? mma_shape<kF16, true>(p, r, grid, stream)
+                                 : mma_shape<kBF16, true>(p, r, grid, stream);
 }
 
 }  // namespace pkv

@@ -555,6 +555,8 @@ __global__ void __launch_bounds__((NC + 1) * 32)
             mbar_arrive(&iq_empty[qs]);
         dec::finish_rows<QT, NC, 1>(p, w, head0, nrows, sm_m, sm_l, sm_acc, ctid, NCT);
     }
+    if (p.wait_prior && ctid == 0)
+        pdl_wait_primary();
 }
 
 std::atomic<unsigned int> g_launch_seq{0};
@@ -617,15 +619,24 @@ cudaError_t run_stream(const DecodeParams& p, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     const int64_t units = p.num_heads;
-    const int64_t items = (int64_t)p.max_partitions * p.num_seqs * units;
+    const int64_t items = (int64_t)p.grid_partitions * p.num_seqs * units;
     if (items <= 0)
         return cudaSuccess;
     if (items > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     const int64_t grid = items < (int64_t)max_ctas ? items : (int64_t)max_ctas;
     const int slot = (int)(g_launch_seq.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
-    kern<<<(unsigned)grid, (NC + 1) * 32, smem, stream>>>(p, (int)items, slot);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((NC + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.wait_prior ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p, (int)items, slot);
 }
 
 template <int CT, int QT, int D>

@@ -1,8 +1,10 @@
 // lse_reduce.cu -- merge of split-context partitions (log-sum-exp reduce).
 //
 // For every (sequence, query head) whose context spans two or more
-// partitions: M = max_p m_p, w_p = 2^(m_p - M),
-// out = sum_p w_p o_p / sum_p w_p l_p.
+// partitions, or that has a shared prefix: M = max_p m_p, w_p = 2^(m_p - M),
+// out = sum_p w_p o_p / sum_p w_p l_p.  With a shared prefix of P tokens the
+// partials are the ceil(P / prefix_partition) partitions of the prefix
+// followed by those of the rest of the context.
 // One warp per (sequence, head) row: lanes read the row's m and l strided,
 // reduce M and the weighted l with shuffles, then every lane accumulates its
 // D/32 output dims over the partitions with independent vector loads.
@@ -12,6 +14,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include "decode_common.cuh"
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
 
@@ -28,13 +31,17 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) lse_reduce_kernel(const Redu
     const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
     const bool live = row < (int64_t)p.num_seqs * p.num_heads;
     int npart = 0;
+    bool merge = false;
     if (live) {
-        const int ctx = __ldg(p.context_lens + row / p.num_heads);
-        if (ctx >= 0 && ctx <= p.max_context_len)
-            npart = (ctx + p.partition_size - 1) / p.partition_size;
+        const int s = (int)(row / p.num_heads);
+        const dec::Split sp = dec::split_context(__ldg(p.context_lens + s),
+                                                 dec::prefix_tokens(p, s), p.max_context_len,
+                                                 p.partition_size, p.prefix_partition);
+        npart = sp.npre + sp.npart;
+        merge = !sp.bad && (sp.pre > 0 || npart > 1);
     }
     pdl_wait_primary();
-    if (npart <= 1)
+    if (!merge)
         return;
 
     const int64_t base = row * p.max_partitions;

@@ -55,12 +55,17 @@ struct WorkspaceLayout {
     int64_t m_off, l_off, o_off, bytes;
 };
 
+// Partials per (sequence, head) row: ceil(max_context_len / partition_size),
+// plus kPrefixParts when shared prefixes are cut into partitions of their own
+// (at most kPrefixParts of them, then ceil((c - P) / ps) <= ceil(c / ps)).
 WorkspaceLayout layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                       int32_t max_context_len, int32_t partition_size)
+                       int32_t max_context_len, int32_t partition_size, bool prefixes = false)
 {
     WorkspaceLayout w{};
     w.parts = partition_size > 0 ? ((int64_t)max_context_len + partition_size - 1) / partition_size
                                  : 0;
+    if (prefixes && w.parts > 0)
+        w.parts += pkv::kPrefixParts;
     if (w.parts <= 1) {
         w.bytes = 0;
         return w;
@@ -99,13 +104,18 @@ int32_t resolve_partition(const pkv_cache_desc* c, int32_t num_seqs, int32_t num
     const int32_t group = c->num_kv_heads > 0 ? num_heads / c->num_kv_heads : 1;
     const bool grouped_items = group >= 2 && group <= 16 && c->cache_dtype != PKV_FP8_E4M3 &&
                                c->block_size % 16 == 0;
-    if (!grouped_items && num_seqs > 0 && num_seqs <= 128 && max_context_len > 0 &&
-        max_context_len <= 8192 &&
-        (int64_t)num_seqs * num_heads >= 6 * (int64_t)device_sms()) {
-        // one partition per context: the streaming kernel takes the longest
-        // contexts first, which balances this many items without a split
+    // one partition per context when there are enough items to fill the GPU:
+    // both kernels take the longest contexts first, which balances this many
+    // items without a split (and the reduce launch disappears).  Items are
+    // (sequence, query head) for the streaming kernel (3 resident per SM, 6
+    // per SM asked) and (sequence, KV head) for the grouped-head kernel
+    // (3 resident per SM, one full wave asked)
+    const int64_t items = grouped_items ? (int64_t)num_seqs * c->num_kv_heads
+                                        : (int64_t)num_seqs * num_heads;
+    const int64_t enough = (grouped_items ? 3 : 6) * (int64_t)device_sms();
+    if (num_seqs > 0 && num_seqs <= 128 && max_context_len > 0 && max_context_len <= 8192 &&
+        items >= enough)
         return (max_context_len + c->block_size - 1) / c->block_size * c->block_size;
-    }
     // K+V bytes of one KV head per partition: 256 KiB when a work item serves
     // one query head, 1 MiB when it serves a group of them
     const int64_t budget = grouped_items ? (1 << 20) : (1 << 18);
@@ -143,12 +153,23 @@ pkv_status decode_checks(const pkv_cache_desc* cache, const void* q, int32_t q_d
     return PKV_OK;
 }
 
-pkv_status launch_partitions(const pkv_cache_desc* cache, const void* q, int32_t q_dtype,
-                             int32_t num_seqs, int32_t num_heads, const int32_t* block_tables,
-                             int32_t max_blocks_per_seq, const int32_t* context_lens,
-                             int32_t max_context_len, float scale, int32_t partition,
-                             void* workspace, const WorkspaceLayout& wl, int32_t* dev_err,
-                             void* out, cudaStream_t stream)
+// Shared-prefix groups of one call (all zero for a plain decode).
+struct Groups {
+    const int32_t* begin;
+    const int32_t* prefix_blocks;
+    int32_t num;
+    int32_t max_size;
+    int32_t max_blocks;
+    int32_t partition;     // prefix_partition
+};
+
+pkv::DecodeParams decode_params(const pkv_cache_desc* cache, const void* q, int32_t q_dtype,
+                                int32_t num_seqs, int32_t num_heads,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t max_context_len,
+                                float scale, int32_t partition, void* workspace,
+                                const WorkspaceLayout& wl, const Groups& grp, int32_t* dev_err,
+                                void* out)
 {
     pkv::DecodeParams p{};
     p.k_cache = cache->k_cache;
@@ -172,6 +193,9 @@ pkv_status launch_partitions(const pkv_cache_desc* cache, const void* q, int32_t
     p.max_context_len = max_context_len;
     p.partition_size = partition;
     p.max_partitions = wl.parts < 1 ? 1 : (int32_t)wl.parts;
+    p.grid_partitions = (int32_t)(((int64_t)max_context_len + partition - 1) / partition);
+    if (p.grid_partitions < 1)
+        p.grid_partitions = 1;
     p.qk_scale_log2 = scale * 1.4426950408889634f * p.k_scale;
     char* ws = reinterpret_cast<char*>(workspace);
     p.ws_m = wl.bytes ? reinterpret_cast<float*>(ws + wl.m_off) : nullptr;
@@ -179,13 +203,34 @@ pkv_status launch_partitions(const pkv_cache_desc* cache, const void* q, int32_t
     p.ws_o = wl.bytes ? reinterpret_cast<float*>(ws + wl.o_off) : nullptr;
     p.dev_err = dev_err;
     p.out = out;
+    p.grp_begin = grp.begin;
+    p.grp_prefix_blocks = grp.prefix_blocks;
+    p.num_groups = grp.num;
+    p.max_group_size = grp.max_size;
+    p.max_prefix_blocks = grp.max_blocks;
+    p.prefix_partition = grp.partition;
+    return p;
+}
+
+pkv_status launch_partitions(const pkv_cache_desc* cache, const void* q, int32_t q_dtype,
+                             int32_t num_seqs, int32_t num_heads, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             int32_t max_context_len, float scale, int32_t partition,
+                             void* workspace, const WorkspaceLayout& wl, int32_t* dev_err,
+                             void* out, cudaStream_t stream, const Groups& grp = Groups{})
+{
+    const pkv::DecodeParams p =
+        decode_params(cache, q, q_dtype, num_seqs, num_heads, block_tables, max_blocks_per_seq,
+                      context_lens, max_context_len, scale, partition, workspace, wl, grp,
+                      dev_err, out);
     return from_cuda(pkv::launch_decode_partitions(p, stream));
 }
 
 pkv_status launch_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
                          const int32_t* context_lens, int32_t max_context_len, int32_t partition,
                          const void* workspace, const WorkspaceLayout& wl, int32_t out_dtype,
-                         void* out, cudaStream_t stream, bool pdl)
+                         void* out, cudaStream_t stream, bool pdl, int32_t block_size = 0,
+                         const Groups& grp = Groups{})
 {
     if (wl.bytes == 0)
         return PKV_OK;
@@ -203,6 +248,13 @@ pkv_status launch_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
     r.ws_o = reinterpret_cast<const float*>(ws + wl.o_off);
     r.out_dtype = out_dtype;
     r.out = out;
+    r.block_size = block_size;
+    r.grp_begin = grp.begin;
+    r.grp_prefix_blocks = grp.prefix_blocks;
+    r.num_groups = grp.num;
+    r.max_group_size = grp.max_size;
+    r.max_prefix_blocks = grp.max_blocks;
+    r.prefix_partition = grp.partition;
     return from_cuda(pkv::launch_lse_reduce(r, stream, pdl));
 }
 
@@ -410,6 +462,85 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, const void* q
         return st;
     return launch_reduce(num_seqs, num_heads, cache->head_dim, context_lens, max_context_len,
                          part, workspace, wl, q_dtype, out, s, true);
+}
+
+size_t pkv_shared_prefix_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
+                                         int32_t num_heads, int32_t max_context_len,
+                                         int32_t partition_size)
+{
+    if (cache == nullptr || cache->block_size <= 0 || cache->head_dim <= 0 || num_seqs <= 0 ||
+        num_heads <= 0 || max_context_len <= 0 || partition_size < 0)
+        return 0;
+    const int32_t part = resolve_partition(cache, num_seqs, num_heads, max_context_len,
+                                           partition_size);
+    return (size_t)layout(num_seqs, num_heads, cache->head_dim, max_context_len, part, true).bytes;
+}
+
+pkv_status pkv_paged_attention_decode_shared_prefix(
+    const pkv_cache_desc* cache, const void* q, int32_t q_dtype, int32_t num_seqs,
+    int32_t num_heads, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t max_context_len, int32_t num_groups,
+    const int32_t* group_begin, const int32_t* group_prefix_blocks, int32_t max_group_size,
+    int32_t max_prefix_blocks, float scale, int32_t partition_size, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* out, pkv_stream_t stream)
+{
+    pkv_status st = decode_checks(cache, q, q_dtype, num_seqs, num_heads, block_tables,
+                                  max_blocks_per_seq, context_lens, max_context_len,
+                                  partition_size, out);
+    if (st != PKV_OK || num_seqs == 0)
+        return st;
+    if (num_groups < 0 || max_group_size < 0 || max_prefix_blocks < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_groups > 0 && (group_begin == nullptr || group_prefix_blocks == nullptr ||
+                           max_group_size == 0 || num_groups > num_seqs))
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)max_prefix_blocks * cache->block_size > max_context_len ||
+        max_prefix_blocks > max_blocks_per_seq)
+        return PKV_ERR_INVALID_ARG;
+    if (!pkv::prefix_kernel_supported(cache->cache_dtype, q_dtype, cache->head_dim,
+                                      cache->block_size, num_heads / cache->num_kv_heads))
+        return PKV_ERR_UNSUPPORTED;
+    const int32_t part = resolve_partition(cache, num_seqs, num_heads, max_context_len,
+                                           partition_size);
+    Groups grp{};
+    if (num_groups > 0 && max_prefix_blocks > 0) {
+        const int32_t bs = cache->block_size;
+        const int32_t tokens = max_prefix_blocks * bs;
+        const int32_t per = (tokens + pkv::kPrefixParts - 1) / pkv::kPrefixParts;
+        const int32_t piece = (per + bs - 1) / bs * bs;
+        grp = Groups{group_begin, group_prefix_blocks, num_groups, max_group_size,
+                     max_prefix_blocks, piece > part ? piece : part};
+    }
+    const bool prefixes = grp.num > 0;
+    const WorkspaceLayout wl =
+        layout(num_seqs, num_heads, cache->head_dim, max_context_len, part, prefixes);
+    st = check_workspace(wl, workspace, workspace_bytes);
+    if (st != PKV_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (prefixes) {
+        const pkv::DecodeParams p =
+            decode_params(cache, q, q_dtype, num_seqs, num_heads, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, part,
+                          workspace, wl, grp, dev_err, out);
+        st = from_cuda(pkv::launch_decode_prefix(p, s));
+        if (st != PKV_OK)
+            return st;
+    }
+    {
+        // the partition kernel overlaps the prefix kernel (it reads nothing the
+        // prefix kernel writes) and waits for it only before it exits
+        pkv::DecodeParams p =
+            decode_params(cache, q, q_dtype, num_seqs, num_heads, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, part,
+                          workspace, wl, grp, dev_err, out);
+        p.wait_prior = prefixes ? 1 : 0;
+        st = from_cuda(pkv::launch_decode_partitions(p, s));
+        if (st != PKV_OK)
+            return st;
+    }
+    return launch_reduce(num_seqs, num_heads, cache->head_dim, context_lens, max_context_len,
+                         part, workspace, wl, q_dtype, out, s, true, cache->block_size, grp);
 }
 
 }  // extern "C"

@@ -27,13 +27,29 @@ struct DecodeParams {
     const int32_t* context_lens;
     int32_t max_context_len;
     int32_t partition_size;
-    int32_t max_partitions;        // ceil(max_context_len / partition_size)
+    int32_t max_partitions;        // partials per (sequence, head) row of the workspace
+    int32_t grid_partitions;       // ceil(max_context_len / partition_size)
     float qk_scale_log2;           // scale * log2(e) * k_scale
     float* ws_m;
     float* ws_l;
     float* ws_o;
     int32_t* dev_err;
     void* out;
+    // Shared prefixes (all null / 0 for a plain decode): sequences
+    // [grp_begin[i], grp_begin[i + 1]) share their first grp_prefix_blocks[i]
+    // blocks.  The prefix kernel covers the first max_group_size members of a
+    // group and prefixes of up to max_prefix_blocks blocks.
+    const int32_t* grp_begin;
+    const int32_t* grp_prefix_blocks;
+    int32_t num_groups;
+    int32_t max_group_size;
+    int32_t max_prefix_blocks;
+    int32_t prefix_partition;      // tokens per partition of a shared prefix
+    // Set when the prefix kernel runs just before: the partition kernel is
+    // then launched with programmatic dependent launch, overlaps it, and waits
+    // for it (griddepcontrol.wait) only before its CTAs exit, so that its own
+    // completion implies the prefix kernel's.
+    int32_t wait_prior;
 };
 
 struct ReduceParams {
@@ -49,6 +65,13 @@ struct ReduceParams {
     const float* ws_o;
     int32_t out_dtype;
     void* out;
+    int32_t block_size;
+    const int32_t* grp_begin;            // shared prefixes, as in DecodeParams
+    const int32_t* grp_prefix_blocks;
+    int32_t num_groups;
+    int32_t max_group_size;
+    int32_t max_prefix_blocks;
+    int32_t prefix_partition;
 };
 
 struct AppendParams {
@@ -71,6 +94,11 @@ struct AppendParams {
 
 constexpr int kCopyMaxLayers = 64;
 
+// Partitions of a shared prefix: prefix_partition = max(partition_size,
+// round_up(ceil(max_prefix_tokens / kPrefixParts), block_size)) tokens, so no
+// row has more than kPrefixParts prefix partials.
+constexpr int kPrefixParts = 4;
+
 struct CopyParams {
     void* k[kCopyMaxLayers];
     void* v[kCopyMaxLayers];
@@ -85,6 +113,11 @@ struct CopyParams {
 // Each returns cudaSuccess, or cudaErrorNotSupported for a shape without a kernel.
 cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_stream(const DecodeParams& p, bool mma, cudaStream_t stream);
+// Partials of the shared prefixes (p.grp_* set); NotSupported unless the cache
+// and q are the same 16-bit type.
+cudaError_t launch_decode_prefix(const DecodeParams& p, cudaStream_t stream);
+bool prefix_kernel_supported(int cache_dtype, int q_dtype, int head_dim, int block_size,
+                             int group);
 cudaError_t launch_lse_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);

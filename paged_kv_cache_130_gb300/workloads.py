@@ -45,7 +45,7 @@ import math
 
 import numpy as np
 
-from .block_manager import BlockManager, BlockPool
+from .block_manager import BlockManager, BlockPool, shared_prefix_groups
 
 F16, BF16, E4M3 = 0, 1, 2
 DTYPE_NAMES = {F16: "f16", BF16: "bf16", E4M3: "e4m3"}
@@ -173,6 +173,11 @@ class Workload:
         tokens = sum(seen.values())
         return tokens * self.num_kv_heads * self.head_dim * 2 * self.cache_elem_bytes
 
+    def prefix_groups(self):
+        """(group_begin, prefix_blocks) of the batch's shared prefixes: runs of
+        consecutive sequences whose block tables start with the same blocks."""
+        return shared_prefix_groups(self.block_tables, self.context_lens, self.block_size)
+
     def append_bytes(self):
         t = int((self.step_slots >= 0).sum())
         per = self.num_kv_heads * self.head_dim * 2 * (self.io_elem_bytes + self.cache_elem_bytes)
@@ -280,7 +285,8 @@ def llama2_7b_fp8_long(seed=5, num_seqs=16, lo=8192, hi=32768, calibrate=True):
 
 def cow_parallel_sampling_f16(seed=4, num_prompts=16, samples=6, prompt_len=504,
                               tail_lo=1, tail_hi=256, num_heads=32, head_dim=128,
-                              block_size=16):
+                              block_size=16, num_kv_heads=None, dtype=F16,
+                              name="cow_parallel_sampling_f16"):
     """Shared prompts with copy-on-write at the first divergent write.
 
     Set-up: each prompt's tokens are written once; ``samples`` sequences share
@@ -320,9 +326,10 @@ def cow_parallel_sampling_f16(seed=4, num_prompts=16, samples=6, prompt_len=504,
     ctx = np.array([s.num_tokens for s in seqs], dtype=np.int64)
     tables = BlockManager.block_table_array(seqs)
     q = _to_bits(_rng(seed, 3).standard_normal((len(seqs), num_heads, head_dim),
-                                                 dtype=np.float32), F16)
-    w = Workload(name="cow_parallel_sampling_f16", seed=seed, cache_dtype=F16, io_dtype=F16,
-                 num_seqs=len(seqs), num_heads=num_heads, num_kv_heads=num_heads,
+                                                 dtype=np.float32), dtype)
+    hkv = num_heads if num_kv_heads is None else num_kv_heads
+    w = Workload(name=name, seed=seed, cache_dtype=dtype, io_dtype=dtype,
+                 num_seqs=len(seqs), num_heads=num_heads, num_kv_heads=hkv,
                  head_dim=head_dim, block_size=block_size, num_blocks=num_blocks,
                  value_sigma=1.0,
                  scale=float(np.float32(1.0) / np.float32(math.sqrt(head_dim))),

@@ -88,6 +88,22 @@ class GpuRun:
                                             self.w.scale, partition_size=ps,
                                             dev_err=self.dev_err)
 
+    def decode_shared(self, partition_size=None, groups=None, max_group_size=None,
+                      max_prefix_blocks=None):
+        """Decode through the shared-prefix entry point; groups default to the
+        batch's own (Workload.prefix_groups)."""
+        w = self.w
+        ps = w.partition_size if partition_size is None else partition_size
+        begin, blocks = w.prefix_groups() if groups is None else groups
+        sizes = np.diff(begin)
+        mgs = int(sizes.max()) if max_group_size is None else max_group_size
+        mpb = int(blocks.max()) if max_prefix_blocks is None else max_prefix_blocks
+        return B.pkv_paged_attention_decode_shared_prefix(
+            self.desc, self.q, self.block_tables, self.context_lens, w.max_context_len,
+            torch.from_numpy(np.ascontiguousarray(begin, np.int32)).to(self.device),
+            torch.from_numpy(np.ascontiguousarray(blocks, np.int32)).to(self.device),
+            mgs, mpb, w.scale, partition_size=ps, dev_err=self.dev_err)
+
     def run_all(self, partition_size=None):
         self.prefill()
         self.copy()

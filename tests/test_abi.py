@@ -44,8 +44,10 @@ def test_partition_size_and_workspace(lib):
     d = _desc()
     # few items: split at 256 KiB of fp16 K+V (512 tokens) per KV head
     assert B.pkv_decode_partition_size(d, 4, 8, 3000, 0) == 512
-    # grouped heads: 1 MiB (2048 tokens)
-    assert B.pkv_decode_partition_size(d, 64, 64, 3000, 0) == 2048
+    # grouped heads, one full wave of (sequence, KV head) items: one partition
+    assert B.pkv_decode_partition_size(d, 64, 64, 3000, 0) == 3008
+    # grouped heads, fewer items: 1 MiB of K+V per partition (2048 tokens)
+    assert B.pkv_decode_partition_size(d, 16, 64, 3000, 0) == 2048
     # many single-head items over short contexts: one partition per context
     d40 = _desc(num_kv_heads=40)
     assert B.pkv_decode_partition_size(d40, 32, 40, 1398, 0) == 1408
@@ -116,3 +118,34 @@ def test_copy_and_reduce_host_checks(lib):
                               ctypes.c_void_p(0x2000), None) == B.PKV_ERR_INVALID_ARG
     assert lib.pkv_lse_reduce(2, 8, 128, ctypes.c_void_p(0x1000), 100, 32, None, 0, 0,
                               ctypes.c_void_p(0x2000), None) == B.PKV_ERR_WORKSPACE
+
+
+def _shared(lib, desc, S=2, H=8, maxctx=64, ng=1, gb=0x8000, gp=0x9000, mgs=2, mpb=2,
+            part=0, ws=None, ws_bytes=0, q_dtype=B.PKV_F16):
+    return lib.pkv_paged_attention_decode_shared_prefix(
+        ctypes.byref(desc), ctypes.c_void_p(0x7000), q_dtype, S, H, ctypes.c_void_p(0x4000), 4,
+        ctypes.c_void_p(0x5000), maxctx, ng, ctypes.c_void_p(gb), ctypes.c_void_p(gp), mgs, mpb,
+        ctypes.c_float(0.1), part, ctypes.c_void_p(ws), ws_bytes, None, ctypes.c_void_p(0x6000),
+        None)
+
+
+def test_shared_prefix_host_checks(lib):
+    d = _desc()
+    # four more partials per row than the plain decode (the prefix pieces)
+    plain = B.pkv_decode_workspace_bytes(d, 4, 8, 3000, 512)
+    shared = B.pkv_shared_prefix_workspace_bytes(d, 4, 8, 3000, 512)
+    s, h, p, dim = 4, 8, 6 + 4, 128
+    ml = -(-4 * s * h * p // 256) * 256
+    assert shared == 2 * ml + -(-4 * s * h * p * dim // 256) * 256 and shared > plain
+    # a context within one partition still needs the workspace with a prefix
+    assert B.pkv_shared_prefix_workspace_bytes(d, 4, 8, 512, 512) > 0
+    assert _shared(lib, _desc(cache_dtype=B.PKV_FP8_E4M3, block_size=32)) == \
+        B.PKV_ERR_UNSUPPORTED
+    assert _shared(lib, d, q_dtype=B.PKV_BF16) == B.PKV_ERR_UNSUPPORTED    # mixed types
+    assert _shared(lib, d, mpb=5) == B.PKV_ERR_INVALID_ARG     # 5 * 16 > max_context_len 64
+    assert _shared(lib, d, mpb=5, maxctx=80) == B.PKV_ERR_INVALID_ARG      # > 4 table entries
+    assert _shared(lib, d, gb=0) == B.PKV_ERR_INVALID_ARG
+    assert _shared(lib, d, ng=3) == B.PKV_ERR_INVALID_ARG      # more groups than sequences
+    assert _shared(lib, d, mgs=0) == B.PKV_ERR_INVALID_ARG
+    assert _shared(lib, d) == B.PKV_ERR_WORKSPACE              # the prefix needs partials
+    assert _shared(lib, d, S=0) == B.PKV_OK

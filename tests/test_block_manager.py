@@ -6,7 +6,8 @@ import os
 import numpy as np
 import pytest
 
-from paged_kv_cache_130_gb300.block_manager import BlockManager, BlockPool, OutOfBlocks
+from paged_kv_cache_130_gb300.block_manager import (BlockManager, BlockPool, OutOfBlocks,
+                                                     shared_prefix_groups)
 from paged_kv_cache_130_gb300 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -105,3 +106,81 @@ def test_cow_workload_counts():
 def test_cow_literal_512_prompt_copies_nothing():
     w = W.cow_parallel_sampling_f16(prompt_len=512, num_prompts=2)
     assert w.copy_pairs.shape == (0, 2)
+
+
+def _check_groups(tables, ctx, bs, begin, prefix):
+    """Every group's prefix is shared, full in every member, and maximal."""
+    assert begin[0] == 0 and begin[-1] == len(ctx)
+    assert np.all(np.diff(begin) >= 1) and len(prefix) == len(begin) - 1
+    for i in range(len(prefix)):
+        a, b, p = begin[i], begin[i + 1], int(prefix[i])
+        if b - a == 1:
+            assert p == 0
+            continue
+        for m in range(a, b):
+            assert np.array_equal(tables[m, :p], tables[a, :p])
+            assert p * bs <= ctx[m]
+        # one more block would break sharing or leave some member's context
+        grows = all(p + 1 <= ctx[m] // bs and tables[m, p] == tables[a, p] for m in range(a, b))
+        assert not grows
+
+
+def test_shared_prefix_groups_of_forked_prompts():
+    w = W.cow_parallel_sampling_f16()
+    begin, prefix = w.prefix_groups()
+    assert np.array_equal(begin, np.arange(0, 97, 6))
+    # 504-token prompts: 31 full shared blocks; the half-full 32nd was copied
+    # by five of the six samples
+    assert np.all(prefix == 31)
+    _check_groups(w.block_tables, w.context_lens, 16, begin, prefix)
+
+
+def test_shared_prefix_groups_without_forks_are_singletons():
+    w = W.opt13b_f16(num_seqs=8)
+    begin, prefix = w.prefix_groups()
+    assert np.array_equal(begin, np.arange(9)) and np.all(prefix == 0)
+
+
+def test_shared_prefix_groups_by_hand():
+    bs = 4
+    pool = BlockPool(64, bs)
+    mgr = BlockManager(pool)
+    a = mgr.new_sequence()
+    mgr.append_tokens(a, 10)                # blocks 0, 1 full, block 2 half
+    forks = [mgr.fork(a) for _ in range(2)]
+    lone = mgr.new_sequence()
+    mgr.append_tokens(lone, 9)
+    c = mgr.new_sequence()
+    mgr.append_tokens(c, 8)                 # exactly two full blocks
+    d = mgr.fork(c)
+    mgr.append_tokens(a, 3)                 # writes into the shared half block: copies
+    mgr.append_tokens(forks[0], 1)
+    mgr.append_tokens(d, 5)
+    seqs = [a] + forks + [lone, c, d]
+    tables = BlockManager.block_table_array(seqs)
+    ctx = np.array([s.num_tokens for s in seqs])
+    begin, prefix = shared_prefix_groups(tables, ctx, bs)
+    assert begin.tolist() == [0, 3, 4, 6]
+    # a's group shares 2 full blocks (the third was half full and is now
+    # copied by a and by forks[0]); c and d share c's 2 blocks
+    assert prefix.tolist() == [2, 0, 2]
+    _check_groups(tables, ctx, bs, begin, prefix)
+
+
+def test_shared_prefix_groups_random_forest():
+    rng = np.random.default_rng(5)
+    bs = 8
+    pool = BlockPool(4096, bs, order=rng.permutation(4096))
+    mgr = BlockManager(pool)
+    seqs = []
+    for _ in range(20):
+        root = mgr.new_sequence()
+        mgr.append_tokens(root, int(rng.integers(1, 60)))
+        group = [root] + [mgr.fork(root) for _ in range(int(rng.integers(0, 4)))]
+        for s in group:
+            mgr.append_tokens(s, int(rng.integers(0, 20)))
+        seqs.extend(group)
+    tables = BlockManager.block_table_array(seqs)
+    ctx = np.array([s.num_tokens for s in seqs])
+    begin, prefix = shared_prefix_groups(tables, ctx, bs)
+    _check_groups(tables, ctx, bs, begin, prefix)
