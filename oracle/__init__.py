@@ -215,3 +215,38 @@ def attention_range(k_cache, v_cache, cache_dtype, q, q_dtype, block_tables, con
     if rc != 0:
         raise ValueError("oracle range attention failed (%d)" % rc)
     return o, m, l
+
+
+def paged_attention_prefill(k_cache, v_cache, cache_dtype, q, q_dtype, cu_seqlens_q,
+                            block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0,
+                            nthreads=0):
+    """Exact causal prefill attention over the paged cache; float64 [total_q, H, D].
+
+    Sequence s brings n_s = cu_seqlens_q[s+1] - cu_seqlens_q[s] new tokens
+    whose K/V are already in the cache as the last n_s of its context_lens[s]
+    tokens (the prompt's K/V are all computed and stored in one pass:
+    「KV Cache从原理到实战」 §2.3).  Query j of sequence s sits at position
+    p = context_lens[s] - n_s + j and, like the decode token, attends to
+    itself and every earlier token (「KV 缓存与分页注意力」 §02): its output is
+    the decode attention of one query over a context of p + 1 tokens.  The
+    oracle therefore expands every query row into one decode row with its
+    sequence's block table and context length p + 1."""
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    cl = np.asarray(context_lens, dtype=np.int64)
+    bt = np.asarray(block_tables, dtype=np.int32)
+    num_seqs = len(cl)
+    if cu.shape != (num_seqs + 1,) or cu[0] != 0 or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens_q must be ascending from 0 with num_seqs + 1 entries")
+    n = np.diff(cu)
+    if np.any(n > cl):
+        raise ValueError("a sequence has more new tokens than context")
+    total = int(cu[-1])
+    if q.shape[0] != total:
+        raise ValueError("q must hold cu_seqlens_q[-1] rows")
+    seq_of_row = np.repeat(np.arange(num_seqs), n)
+    j = np.arange(total) - cu[seq_of_row]
+    pos = cl[seq_of_row] - n[seq_of_row] + j
+    rows_bt = bt[seq_of_row] if total else np.zeros((0, bt.shape[1]), np.int32)
+    return paged_attention_decode(k_cache, v_cache, cache_dtype, q, q_dtype, rows_bt,
+                                  (pos + 1).astype(np.int32), scale, k_scale, v_scale,
+                                  nthreads)
