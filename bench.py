@@ -192,6 +192,17 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ peaks
 
+def tensor_peak():
+    """Measured dense bf16 TFLOP/s (burst: the kernel is timed alone); fp16 runs
+    at the same nominal rate on this part."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -567,6 +578,209 @@ def run_gpu(args, w, prefill):
     return line if rank == 0 else None
 
 
+# ------------------------------------------------------------------ prefill arm
+
+PREFILL_METRIC = "paged prefill attention TFLOP/s (causal, new tokens over the paged cache)"
+
+
+def prefill_oracle_rows(w, hs, rows):
+    """Time the oracle's prefill of query `rows` (each the decode of its
+    position's causal context); returns (seconds, flops of those rows)."""
+    import oracle
+    cu = w.cu_seqlens_q.astype(np.int64)
+    seq = np.searchsorted(cu, rows, side="right") - 1
+    n = cu[seq + 1] - cu[seq]
+    pos = w.context_lens[seq].astype(np.int64) - n + (rows - cu[seq])
+    t0 = time.perf_counter()
+    oracle.paged_attention_decode(hs.k_cache, hs.v_cache, w.cache_dtype, w.q[rows], w.io_dtype,
+                                  w.block_tables[seq], (pos + 1).astype(np.int32), w.scale)
+    t = time.perf_counter() - t0
+    return t, int(4 * (pos + 1).sum() * w.head_dim * w.num_heads)
+
+
+def prefill_cpu_sample(w, hs, budget_s):
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(w.total_q, min(w.total_q, 16), replace=False))
+    t, f = prefill_oracle_rows(w, hs, rows)
+    n = int(min(w.total_q, max(16, len(rows) * budget_s / max(t, 1e-3))))
+    rows = np.sort(rng.choice(w.total_q, n, replace=False))
+    return rows
+
+
+def run_reference_prefill(args, w, prefill):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    hs = HostState(w, prefill)
+    cores = os.cpu_count() or 1
+    rows = prefill_cpu_sample(w, hs, 20.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        prefill_oracle_rows(w, hs, rows)
+    tot_t, tot_f = 0.0, 0
+    for _ in range(args.steps):
+        t, f = prefill_oracle_rows(w, hs, rows)
+        tot_t += t
+        tot_f += f
+    v = tot_f / tot_t / 1e12
+    return {"metric": PREFILL_METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_t * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": prefill_config(w),
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "%d of %d query rows per step" % (len(rows), w.total_q)},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def prefill_config(w):
+    cfg = workload_config(w)
+    cfg.update({"new_tokens": w.total_q, "max_q_len": w.max_q_len,
+                "cached_tokens": int(w.context_lens.sum()) - w.total_q,
+                "l2": "K/V of the batch (%.0f MB) are read once per 64-row query tile; "
+                      "compute-bound, no flush" % (w.kv_bytes() / 1e6)})
+    return cfg
+
+
+def run_gpu_prefill(args, w, prefill):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_cache_130_gb300 import binding as B
+    from paged_kv_cache_130_gb300 import build as pkv_build
+
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+    pkv_build.build()
+    B.load()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    dt = {0: torch.float16, 1: torch.bfloat16}[w.io_dtype]
+    k_cache = torch.zeros(shape, dtype=dt, device=dev)
+    v_cache = torch.zeros(shape, dtype=dt, device=dev)
+    desc = B.cache_desc(k_cache, v_cache)
+
+    def dev16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(dt).to(dev)
+
+    for slots, k, v in prefill:
+        B.pkv_kv_append(desc, dev16(k), dev16(v), torch.from_numpy(slots).to(dev))
+    sk, sv = w.step_values()
+    step_k, step_v = dev16(sk), dev16(sv)
+    step_slots = torch.from_numpy(w.step_slots).to(dev)
+    q = dev16(w.q)
+    cu = torch.from_numpy(w.cu_seqlens_q).to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    out = torch.empty_like(q)
+    flops = w.prefill_flops()
+
+    def pre():
+        B.pkv_kv_append(desc, step_k, step_v, step_slots)
+
+    def attn():
+        B.pkv_paged_attention_prefill(desc, q, cu, w.max_q_len, bt, cl, w.max_context_len,
+                                      w.scale, out=out)
+
+    for _ in range(args.warmup):
+        pre()
+        attn()
+    torch.cuda.synchronize()
+    replay = {"pre": pre, "attn": attn}
+    if not args.no_graphs:
+        for name, fn in list(replay.items()):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            replay[name] = g.replay
+        torch.cuda.synchronize()
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record()
+        replay["pre"]()
+        e1.record()
+        replay["attn"]()
+        e2.record()
+        evs.append((e0, e1, e2))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    attn_s = sum(b.elapsed_time(c) for _, b, c in evs) / 1e3
+    step_s = sum(a.elapsed_time(c) for a, _, c in evs) / 1e3
+    attn_s, step_s = slowest([attn_s, step_s], dev)
+    value = whole_job_rate(flops * args.steps, attn_s, world) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        h = {"q": w.q, "k": sk, "v": sv}
+        hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(h[x]).view(np.int16)).view(dt)
+                      .pin_memory() for x in ("q", "k", "v"))
+        hslots = torch.from_numpy(w.step_slots).pin_memory()
+        hcu = torch.from_numpy(w.cu_seqlens_q).pin_memory()
+        hbt = torch.from_numpy(w.block_tables).pin_memory()
+        hcl = torch.from_numpy(w.context_lens).pin_memory()
+        hout = torch.empty(out.shape, dtype=dt).pin_memory()
+        ins = (hq, hk, hv, hslots, hcu, hbt, hcl)
+        h2d = sum(t.numel() * t.element_size() for t in ins)
+        d2h = hout.numel() * hout.element_size()
+        ms = []
+        for i in range(args.steps + args.warmup):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for dst, src in zip((q, step_k, step_v, step_slots, cu, bt, cl), ins):
+                dst.copy_(src, non_blocking=True)
+            pre()
+            attn()
+            hout.copy_(out, non_blocking=True)
+            b.record()
+            b.synchronize()
+            if i >= args.warmup:
+                ms.append(a.elapsed_time(b))
+        e2e_s = slowest([sum(ms) / 1e3], dev)[0]
+        e2e = {"value": whole_job_rate(flops * args.steps, e2e_s, world) / 1e12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_s * 1e3 / args.steps}
+
+    peak, kind = tensor_peak()
+    achieved = flops / (attn_s / args.steps) / 1e12
+    line = {"metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {0: "f16", 1: "bf16"}[w.io_dtype], "data": "synthetic",
+            "config": prefill_config(w),
+            "prefill_flops": flops,
+            "step_ms": {"append": sum(a.elapsed_time(b) for a, b, _ in evs) / args.steps,
+                        "prefill": attn_s * 1e3 / args.steps},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "kernel": "prefill_kernel (pkv_paged_attention_prefill)",
+                         "peak_source": kind + " (MEASURED_PEAKS.json bf16_tflops, burst)"
+                         if kind == "measured" else "fallback 1.9 PFLOP/s"},
+            "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk}
+    if rank == 0 and not args.no_cpu_baseline:
+        hs = HostState(w, prefill)
+        rows = prefill_cpu_sample(w, hs, 15.0)
+        t, f = prefill_oracle_rows(w, hs, rows)
+        line["cpu_baseline"] = {"value": f / t / 1e12, "unit": "TFLOP/s",
+                                "cores": os.cpu_count() or 1, "kind": "oracle",
+                                "sample": "%d of %d query rows" % (len(rows), w.total_q)}
+    return line if rank == 0 else None
+
+
 def main(argv=None):
     args = parse_args(argv)
     from paged_kv_cache_130_gb300 import workloads as W
@@ -575,10 +789,11 @@ def main(argv=None):
         return 0
     w = W.make(args.workload)
     prefill = list(w.prefill())
-    if args.impl == "reference":
-        line = run_reference(args, w, prefill)
+    if w.cu_seqlens_q is not None:
+        run = run_reference_prefill if args.impl == "reference" else run_gpu_prefill
     else:
-        line = run_gpu(args, w, prefill)
+        run = run_reference if args.impl == "reference" else run_gpu
+    line = run(args, w, prefill)
     if line is not None:
         print(json.dumps(line), flush=True)
     return 0

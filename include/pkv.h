@@ -287,6 +287,42 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
     size_t workspace_bytes, int32_t* dev_err, void* out, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Prefill attention -- the prompt phase: all new tokens of each sequence
+ * attend causally over the paged cache (「KV Cache从原理到实战」 §2.3: the
+ * prompt's K and V are computed and stored in one pass; 「KV 缓存与分页注意力」
+ * §02: a token attends to itself and every earlier token).
+ *
+ * The new tokens' K/V must already be in the cache (pkv_kv_append), as the
+ * last n_s of each context.  For sequence s, n_s = cu_seqlens_q[s + 1] -
+ * cu_seqlens_q[s] and c = context_lens[s]; query row cu_seqlens_q[s] + j
+ * (j < n_s) sits at position p = c - n_s + j and
+ *   out[row][h][:] = sum_{t <= p} exp(x_t - max x) v_t / sum_{t <= p} exp(x_t - max x),
+ *   x_t = scale * dot(q[row][h], k_t),  k_t, v_t of KV head h / (num_heads / num_kv_heads)
+ * with fp32 accumulation, rounded once to q_dtype.  A context cached before
+ * the new tokens (chunked prefill) is attended to like the rest.
+ *
+ * q, out        device [total_q][num_heads][head_dim] of q_dtype, 16-byte aligned.
+ * cu_seqlens_q  device int32 [num_seqs + 1], ascending from 0 to total_q.
+ * max_q_len     host upper bound of n_s (sizes the grid).
+ * block_tables, context_lens, max_context_len: as for the decode.
+ * Supported: F16 or BF16 caches with q of the same type, head_dim 64 or 128,
+ *   block_size 8, 16 or 32, 1..64 query heads per KV head; others return
+ *   PKV_ERR_UNSUPPORTED.
+ * Device checks (with dev_err): n_s above max_q_len or c, c above
+ *   max_context_len or the table, bad cu_seqlens_q -> PKV_DEVERR_CONTEXT (that
+ *   sequence's rows are zero, or untouched when cu_seqlens_q is bad); a bad block
+ *   id -> PKV_DEVERR_BLOCK_ID (the key is read as zeros).
+ * Launches: one kernel.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_attention_prefill(const pkv_cache_desc* cache, const void* q,
+                                       int32_t q_dtype, int32_t num_seqs, int32_t num_heads,
+                                       const int32_t* cu_seqlens_q, int32_t total_q,
+                                       int32_t max_q_len, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t max_context_len, float scale, int32_t* dev_err,
+                                       void* out, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * pkv_paged_attention_decode_static_ws -- the decode above for callers that
  * cannot allocate device memory.  The pages have no counterpart: this is a
  * deployment convenience of the library, not part of the method.

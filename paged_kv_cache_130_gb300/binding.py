@@ -74,6 +74,8 @@ def load():
         "pkv_paged_attention_decode_static_ws": (i32, [dp, vp, i32, i32, i32, vp, i32, vp, i32,
                                                        f32, i32, vp, vp, vp]),
         "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [dp, i32, i32, i32, i32]),
+        "pkv_paged_attention_prefill": (i32, [dp, vp, i32, i32, i32, vp, i32, i32, vp, i32,
+                                              vp, i32, f32, vp, vp, vp]),
         "pkv_paged_attention_decode_shared_prefix": (i32, [dp, vp, i32, i32, i32, vp, i32, vp,
                                                            i32, i32, vp, vp, i32, i32, f32, i32,
                                                            vp, ctypes.c_size_t, vp, vp, vp]),
@@ -290,5 +292,29 @@ def pkv_paged_attention_decode_shared_prefix(cache, q, block_tables, context_len
         _ptr(group_begin), _ptr(group_prefix_blocks), int(max_group_size),
         int(max_prefix_blocks), float(scale), int(partition_size), _ptr(workspace), ws_bytes,
         _ptr(dev_err), _ptr(out), _stream(stream)), "pkv_paged_attention_decode_shared_prefix")
+    return out
+
+
+def pkv_paged_attention_prefill(cache, q, cu_seqlens_q, max_q_len, block_tables, context_lens,
+                                max_context_len, scale, dev_err=None, out=None, stream=None):
+    """Causal prefill of q [total_q, num_heads, head_dim]: sequence s owns rows
+    [cu_seqlens_q[s], cu_seqlens_q[s+1]), the last tokens of its context."""
+    _dense(q, "q")
+    for t, name in ((cu_seqlens_q, "cu_seqlens_q"), (block_tables, "block_tables"),
+                    (context_lens, "context_lens")):
+        _dense(t, name)
+        if t.dtype != torch.int32:
+            raise ValueError("%s must be int32" % name)
+    total, h, d = q.shape
+    num_seqs = context_lens.numel()
+    if cu_seqlens_q.numel() != num_seqs + 1:
+        raise ValueError("cu_seqlens_q needs num_seqs + 1 entries")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().pkv_paged_attention_prefill(
+        ctypes.byref(cache), _ptr(q), dtype_code(q.dtype), num_seqs, h, _ptr(cu_seqlens_q),
+        total, int(max_q_len), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        int(max_context_len), float(scale), _ptr(dev_err), _ptr(out), _stream(stream)),
+        "pkv_paged_attention_prefill")
     return out
 

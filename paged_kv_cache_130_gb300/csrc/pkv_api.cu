@@ -543,4 +543,54 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
                          part, workspace, wl, q_dtype, out, s, true, cache->block_size, grp);
 }
 
+pkv_status pkv_paged_attention_prefill(const pkv_cache_desc* cache, const void* q,
+                                       int32_t q_dtype, int32_t num_seqs, int32_t num_heads,
+                                       const int32_t* cu_seqlens_q, int32_t total_q,
+                                       int32_t max_q_len, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t max_context_len, float scale, int32_t* dev_err,
+                                       void* out, pkv_stream_t stream)
+{
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK)
+        return st;
+    if (num_seqs < 0 || num_heads <= 0 || total_q < 0 || max_q_len < 0 ||
+        max_blocks_per_seq < 0 || max_context_len < 0 || !is16(q_dtype))
+        return PKV_ERR_INVALID_ARG;
+    if (num_heads % cache->num_kv_heads != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0 || max_q_len == 0)
+        return PKV_OK;
+    if (q == nullptr || out == nullptr || cu_seqlens_q == nullptr || context_lens == nullptr ||
+        block_tables == nullptr || max_blocks_per_seq == 0 || !aligned16(q) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    if (!pkv::prefill_shape_supported(cache->cache_dtype, cache->head_dim, cache->block_size,
+                                      num_heads / cache->num_kv_heads) ||
+        q_dtype != cache->cache_dtype)
+        return PKV_ERR_UNSUPPORTED;
+    pkv::PrefillParams p{};
+    p.k_cache = cache->k_cache;
+    p.v_cache = cache->v_cache;
+    p.num_blocks = cache->num_blocks;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.block_size = cache->block_size;
+    p.head_dim = cache->head_dim;
+    p.dtype = cache->cache_dtype;
+    p.q = q;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.group = num_heads / cache->num_kv_heads;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.total_q = total_q;
+    p.max_q_len = max_q_len;
+    p.block_tables = block_tables;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.max_context_len = max_context_len;
+    p.qk_scale_log2 = scale * 1.4426950408889634f;
+    p.dev_err = dev_err;
+    p.out = out;
+    return from_cuda(pkv::launch_prefill(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

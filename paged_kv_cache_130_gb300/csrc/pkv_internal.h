@@ -94,6 +94,33 @@ struct AppendParams {
 
 constexpr int kCopyMaxLayers = 64;
 
+struct PrefillParams {
+    const void* k_cache;
+    const void* v_cache;
+    int64_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t head_dim;
+    int32_t dtype;                 // cache, q and out (F16 or BF16)
+    const void* q;                 // [total_q][num_heads][head_dim]
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t group;
+    const int32_t* cu_seqlens_q;   // [num_seqs + 1]
+    int32_t total_q;               // rows of q and out
+    int32_t max_q_len;
+    const int32_t* block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t* context_lens;
+    int32_t max_context_len;
+    float qk_scale_log2;           // scale * log2(e)
+    int32_t* dev_err;
+    void* out;                     // [total_q][num_heads][head_dim]
+};
+
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+bool prefill_shape_supported(int dtype, int head_dim, int block_size, int group);
+
 // Partitions of a shared prefix: prefix_partition = max(partition_size,
 // round_up(ceil(max_prefix_tokens / kPrefixParts), block_size)) tokens, so no
 // row has more than kPrefixParts prefix partials.

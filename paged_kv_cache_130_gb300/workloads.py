@@ -108,6 +108,9 @@ class Workload:
     k_scale: float = 1.0
     v_scale: float = 1.0
     notes: dict = field(default_factory=dict)
+    # prefill workloads: int32 [S + 1]; q is then [total_q, H, D] and the step
+    # appends every new token before the prefill attention
+    cu_seqlens_q: np.ndarray = None
 
     # ------------------------------------------------------------ values
     def values(self, key, n):
@@ -177,6 +180,26 @@ class Workload:
         """(group_begin, prefix_blocks) of the batch's shared prefixes: runs of
         consecutive sequences whose block tables start with the same blocks."""
         return shared_prefix_groups(self.block_tables, self.context_lens, self.block_size)
+
+    def prefill_flops(self):
+        """Multiply-adds x 2 of the causal prefill: query j of sequence s at
+        position p reads p + 1 keys and values, 2 (p + 1) D MACs per head."""
+        cu = self.cu_seqlens_q.astype(np.int64)
+        ctx = self.context_lens.astype(np.int64)
+        total = 0
+        for s in range(self.num_seqs):
+            n = int(cu[s + 1] - cu[s])
+            first = int(ctx[s]) - n + 1               # keys of the first new token
+            total += n * first + n * (n - 1) // 2     # sum of keys over the n rows
+        return 4 * total * self.head_dim * self.num_heads
+
+    @property
+    def max_q_len(self):
+        return int(np.diff(self.cu_seqlens_q).max()) if self.num_seqs else 0
+
+    @property
+    def total_q(self):
+        return int(self.cu_seqlens_q[-1])
 
     def append_bytes(self):
         t = int((self.step_slots >= 0).sum())
@@ -341,6 +364,66 @@ def cow_parallel_sampling_f16(seed=4, num_prompts=16, samples=6, prompt_len=504,
     return w
 
 
+def _prompts(name, seed, dtype, num_heads, num_kv_heads, head_dim, block_size, new, cached,
+             max_seg_tokens=4096):
+    """Prompt-phase batches: sequence i holds cached[i] tokens from earlier
+    chunks (written in the set-up), the step appends its new[i] tokens, then
+    the prefill attention runs for the new tokens."""
+    new = np.asarray(new, dtype=np.int64)
+    cached = np.asarray(cached, dtype=np.int64)
+    ctx = new + cached
+    need = int(((ctx + block_size - 1) // block_size).sum())
+    num_blocks = int(math.ceil(1.25 * need))
+    pool, mgr = _pool_and_manager(num_blocks, block_size, seed)
+    seqs = [mgr.new_sequence() for _ in ctx]
+    segments, step = [], []
+    for i, s in enumerate(seqs):
+        slots, _ = mgr.append_tokens(s, int(cached[i]))
+        for j in range(0, len(slots), max_seg_tokens):
+            segments.append(Segment(key=(1, i, j // max_seg_tokens),
+                                    slots=slots[j:j + max_seg_tokens]))
+    for s, n in zip(seqs, new):
+        slots, _ = mgr.append_tokens(s, int(n))
+        step.append(slots)
+    tables = BlockManager.block_table_array(seqs)
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    q = _to_bits(_rng(seed, 3).standard_normal((int(cu[-1]), num_heads, head_dim),
+                                                 dtype=np.float32), dtype)
+    w = Workload(name=name, seed=seed, cache_dtype=dtype, io_dtype=dtype,
+                 num_seqs=len(seqs), num_heads=num_heads, num_kv_heads=num_kv_heads,
+                 head_dim=head_dim, block_size=block_size, num_blocks=num_blocks,
+                 value_sigma=1.0,
+                 scale=float(np.float32(1.0) / np.float32(math.sqrt(head_dim))),
+                 partition_size=0, context_lens=ctx.astype(np.int32), block_tables=tables,
+                 q=q, segments=segments, step_slots=np.concatenate(step), step_key=(2,),
+                 copy_pairs=np.zeros((0, 2), dtype=np.int64), cu_seqlens_q=cu)
+    w.notes["pool_blocks"] = num_blocks
+    return w
+
+
+def prefill_llama2_7b_bf16(seed=6, num_seqs=8, lo=512, hi=2048, num_heads=32,
+                           num_kv_heads=32, head_dim=128, block_size=16, dtype=BF16):
+    """Llama-2-7B attention layer shape, whole prompts of U[lo, hi] tokens."""
+    new = _rng(seed, 0).integers(lo, hi, size=num_seqs, endpoint=True)
+    return _prompts("prefill_llama2_7b_bf16", seed, dtype, num_heads, num_kv_heads, head_dim,
+                    block_size, new, np.zeros(num_seqs, np.int64))
+
+
+def prefill_llama2_70b_gqa_chunked_bf16(seed=7, num_seqs=4, chunk=512, lo=1024, hi=4096,
+                                        block_size=16):
+    """Llama-2-70B layer shape (64 query heads over 8 KV heads), chunked
+    prefill: U[lo, hi] tokens already cached, then a chunk of new tokens."""
+    cached = _rng(seed, 0).integers(lo, hi, size=num_seqs, endpoint=True)
+    return _prompts("prefill_llama2_70b_gqa_chunked_bf16", seed, BF16, 64, 8, 128, block_size,
+                    np.full(num_seqs, chunk, np.int64), cached)
+
+
+PREFILL_WORKLOADS = {
+    "prefill_llama2_7b_bf16": prefill_llama2_7b_bf16,
+    "prefill_llama2_70b_gqa_chunked_bf16": prefill_llama2_70b_gqa_chunked_bf16,
+}
+
+
 WORKLOADS = {
     "tiny_f16": tiny_f16,
     "opt13b_f16": opt13b_f16,
@@ -351,4 +434,6 @@ WORKLOADS = {
 
 
 def make(name, **kw):
+    if name in PREFILL_WORKLOADS:
+        return PREFILL_WORKLOADS[name](**kw)
     return WORKLOADS[name](**kw)

@@ -104,6 +104,14 @@ class GpuRun:
             torch.from_numpy(np.ascontiguousarray(blocks, np.int32)).to(self.device),
             mgs, mpb, w.scale, partition_size=ps, dev_err=self.dev_err)
 
+    def prefill_attention(self):
+        """Causal prefill of the workload's new tokens (after step())."""
+        w = self.w
+        cu = torch.from_numpy(w.cu_seqlens_q).to(self.device)
+        return B.pkv_paged_attention_prefill(self.desc, self.q, cu, w.max_q_len,
+                                             self.block_tables, self.context_lens,
+                                             w.max_context_len, w.scale, dev_err=self.dev_err)
+
     def run_all(self, partition_size=None):
         self.prefill()
         self.copy()
@@ -149,6 +157,23 @@ class OracleRun:
             q, bt, cl = q[seqs], bt[seqs], cl[seqs]
         return oracle.paged_attention_decode(self.k_cache, self.v_cache, w.cache_dtype, q,
                                              w.io_dtype, bt, cl, w.scale, w.k_scale, w.v_scale)
+
+    def prefill_attention(self, rows=None):
+        """Oracle prefill of the new tokens; `rows` picks query rows (each is
+        the decode of its position's causal context)."""
+        w = self.w
+        if rows is None:
+            return oracle.paged_attention_prefill(
+                self.k_cache, self.v_cache, w.cache_dtype, w.q, w.io_dtype, w.cu_seqlens_q,
+                w.block_tables, w.context_lens, w.scale, w.k_scale, w.v_scale)
+        cu = w.cu_seqlens_q.astype(np.int64)
+        rows = np.asarray(rows, dtype=np.int64)
+        seq = np.searchsorted(cu, rows, side="right") - 1
+        n = cu[seq + 1] - cu[seq]
+        pos = w.context_lens[seq].astype(np.int64) - n + (rows - cu[seq])
+        return oracle.paged_attention_decode(
+            self.k_cache, self.v_cache, w.cache_dtype, w.q[rows], w.io_dtype,
+            w.block_tables[seq], (pos + 1).astype(np.int32), w.scale, w.k_scale, w.v_scale)
 
     def run_all(self):
         self.prefill()
