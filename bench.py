@@ -781,6 +781,192 @@ def run_gpu_prefill(args, w, prefill):
     return line if rank == 0 else None
 
 
+# ------------------------------------------------------------------ swap arm
+
+SWAP_METRIC = "block swap GB/s (device cache <-> pinned host memory, out + in)"
+
+
+def swap_oracle_sample(w, layers=2):
+    """Oracle swap of `layers` layers of the workload on host arrays; returns
+    (seconds, bytes moved)."""
+    import oracle
+    shape = (w.num_kv_heads, w.block_size, w.head_dim)
+    dk = [np.full((w.num_blocks,) + shape, l + 1, np.uint16) for l in range(layers)]
+    dv = [np.full((w.num_blocks,) + shape, l + 2, np.uint16) for l in range(layers)]
+    # written before the clock starts, so that first-touch page faults stay out
+    hk = [np.full((w.host_blocks,) + shape, 0, np.uint16) for _ in range(layers)]
+    hv = [np.full((w.host_blocks,) + shape, 0, np.uint16) for _ in range(layers)]
+    t0 = time.perf_counter()
+    oracle.swap_blocks(dk, dv, hk, hv, w.out_pairs)
+    oracle.swap_blocks(hk, hv, dk, dv, w.in_pairs)
+    t = time.perf_counter() - t0
+    return t, w.swap_bytes() * layers // w.num_layers
+
+
+def swap_config(w):
+    return {"workload": w.name, "num_layers": w.num_layers, "num_blocks": w.num_blocks,
+            "host_blocks": w.host_blocks, "num_kv_heads": w.num_kv_heads,
+            "block_size": w.block_size, "head_dim": w.head_dim, "cache_dtype": "f16",
+            "swapped_sequences": int(len(w.swapped_seqs)), "pairs_each_way": int(len(w.out_pairs)),
+            "block_bytes": w.block_bytes,
+            "l2": "%.1f GB moved per step exceeds the 129 MB L2" % (w.swap_bytes() / 1e9),
+            "parallelism": "replicas"}
+
+
+def run_reference_swap(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        swap_oracle_sample(w)
+    tt, bb = 0.0, 0
+    for _ in range(args.steps):
+        t, b = swap_oracle_sample(w)
+        tt += t
+        bb += b
+    v = bb / tt / 1e9
+    return {"metric": SWAP_METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic", "impl": "reference", "config": swap_config(w),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "2 of %d layers per step" % w.num_layers},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_gpu_swap(args, w):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_cache_130_gb300 import binding as B
+    from paged_kv_cache_130_gb300 import build as pkv_build
+
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+    pkv_build.build()
+    B.load()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    shape = (w.num_kv_heads, w.block_size, w.head_dim)
+    dk = [torch.full((w.num_blocks,) + shape, float(l), dtype=torch.float16, device=dev)
+          for l in range(w.num_layers)]
+    dv = [torch.full((w.num_blocks,) + shape, -float(l), dtype=torch.float16, device=dev)
+          for l in range(w.num_layers)]
+    hk = [torch.empty((w.host_blocks,) + shape, dtype=torch.float16).pin_memory()
+          for _ in range(w.num_layers)]
+    hv = [torch.empty((w.host_blocks,) + shape, dtype=torch.float16).pin_memory()
+          for _ in range(w.num_layers)]
+    ddesc = [B.cache_desc(a, b) for a, b in zip(dk, dv)]
+    hdesc = [B.cache_desc(a, b) for a, b in zip(hk, hv)]
+    p_out = torch.from_numpy(w.out_pairs).to(dev)
+    p_in = torch.from_numpy(w.in_pairs).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def out():
+        B.pkv_swap_blocks(ddesc, hdesc, p_out, dev_err=err)
+
+    def back():
+        B.pkv_swap_blocks(hdesc, ddesc, p_in, dev_err=err)
+
+    for _ in range(args.warmup):
+        out()
+        back()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record()
+        out()
+        e1.record()
+        back()
+        e2.record()
+        evs.append((e0, e1, e2))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    out_s = sum(a.elapsed_time(b) for a, b, _ in evs) / 1e3
+    in_s = sum(b.elapsed_time(c) for _, b, c in evs) / 1e3
+    out_s, in_s = slowest([out_s, in_s], dev)
+    moved = w.swap_bytes()
+    value = whole_job_rate(moved * args.steps, out_s + in_s, world) / 1e9
+
+    # the copy engines' rate on one large pinned buffer, each way: the link's
+    # measured ceiling for this run
+    nbytes = 2 << 30
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    hbuf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    rates = []
+    for direction in ("d2h", "h2d"):
+        best = 0.0
+        for _ in range(3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            if direction == "d2h":
+                hbuf.copy_(dbuf, non_blocking=True)
+            else:
+                dbuf.copy_(hbuf, non_blocking=True)
+            b.record()
+            b.synchronize()
+            best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+        rates.append(best)
+    peak = 2.0 / (1.0 / rates[0] + 1.0 / rates[1])      # out and in take equal bytes
+
+    e2e = None
+    if not args.no_e2e:
+        hp_out = torch.from_numpy(w.out_pairs).pin_memory()
+        hp_in = torch.from_numpy(w.in_pairs).pin_memory()
+        herr = torch.zeros(1, dtype=torch.int32).pin_memory()
+        ms = []
+        for i in range(args.steps + args.warmup):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            p_out.copy_(hp_out, non_blocking=True)
+            p_in.copy_(hp_in, non_blocking=True)
+            out()
+            back()
+            herr.copy_(err, non_blocking=True)
+            b.record()
+            b.synchronize()
+            if i >= args.warmup:
+                ms.append(a.elapsed_time(b))
+        e2e_s = slowest([sum(ms) / 1e3], dev)[0]
+        e2e = {"value": whole_job_rate(moved * args.steps, e2e_s, world) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(moved // 2 + 16 * len(w.out_pairs)),
+               "d2h_bytes_per_step": int(moved // 2 + 4),
+               "ms_per_step": e2e_s * 1e3 / args.steps}
+    line = {"metric": SWAP_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": (out_s + in_s) * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": swap_config(w), "swap_bytes_per_step": moved,
+            "step_ms": {"out": out_s * 1e3 / args.steps, "in": in_s * 1e3 / args.steps},
+            "roofline": {"bound": "c2c", "achieved": value, "peak": peak, "unit": "GB/s",
+                         "frac": value / peak, "traffic": None,
+                         "kernel": "swap_blocks_kernel (pkv_swap_blocks, both directions)",
+                         "peak_source": "measured in this run: cudaMemcpyAsync of 2 GiB "
+                                        "pinned, D2H %.0f GB/s and H2D %.0f GB/s" % tuple(rates)},
+            "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
+            "dev_err": int(err.item())}
+    if rank == 0 and not args.no_cpu_baseline:
+        t, b = swap_oracle_sample(w)
+        line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": "2 of %d layers" % w.num_layers}
+    return line if rank == 0 else None
+
+
 def main(argv=None):
     args = parse_args(argv)
     from paged_kv_cache_130_gb300 import workloads as W
@@ -788,6 +974,11 @@ def main(argv=None):
     if args.impl == "reference" and rank != 0:
         return 0
     w = W.make(args.workload)
+    if isinstance(w, W.SwapWorkload):
+        line = (run_reference_swap if args.impl == "reference" else run_gpu_swap)(args, w)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
     prefill = list(w.prefill())
     if w.cu_seqlens_q is not None:
         run = run_reference_prefill if args.impl == "reference" else run_gpu_prefill

@@ -142,6 +142,30 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* caches, int32_t num_layers,
                            int32_t* dev_err, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Block swap -- move whole blocks between two pools, typically the device
+ * cache and a pool in pinned host memory: a pre-empted sequence's blocks go to
+ * CPU memory and come back when it runs again (「KV 缓存与分页注意力」 §09).
+ *
+ * For each pair i and each layer l:
+ *   dst[l].k_cache[pairs[i][1]] = src[l].k_cache[pairs[i][0]]  (and v_cache)
+ * byte for byte; a block is num_kv_heads * block_size * head_dim elements.
+ * src, dst        host arrays of num_layers descriptors; every layer of a side
+ *                 has the same shape and pool size, and both sides the same
+ *                 block shape and element type.  Each cache pointer must be
+ *                 device memory or pinned, device-mapped host memory (checked
+ *                 with cudaPointerGetAttributes; anything else returns
+ *                 PKV_ERR_INVALID_ARG before any launch).  On GB300 the kernel
+ *                 reads and writes the host side directly over NVLink-C2C.
+ * block_pairs     int64 [num_pairs][2] (src block, dst block), device or
+ *                 pinned host memory; dst blocks must be distinct.
+ * A pair outside its pool is skipped and flags PKV_DEVERR_COPY_PAIR.
+ * Launches: one kernel per 64 layers and 65,535 pairs.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_swap_blocks(const pkv_cache_desc* src, const pkv_cache_desc* dst,
+                           int32_t num_layers, const int64_t* block_pairs, int64_t num_pairs,
+                           int32_t* dev_err, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Decode attention -- one query token per sequence attends over its whole
  * cached context, which the kernel reads block by block through the table.
  *   「KV 缓存与分页注意力」 §02 and §07; grouped heads: §11.

@@ -250,3 +250,23 @@ def paged_attention_prefill(k_cache, v_cache, cache_dtype, q, q_dtype, cu_seqlen
     return paged_attention_decode(k_cache, v_cache, cache_dtype, q, q_dtype, rows_bt,
                                   (pos + 1).astype(np.int32), scale, k_scale, v_scale,
                                   nthreads)
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs):
+    """Block swap between two pools (device cache <-> host memory), in place.
+
+    When blocks run short, all of a sequence's blocks move to CPU memory and
+    come back when the sequence runs again (「KV 缓存与分页注意力」 §09).  For each
+    (src, dst) pair and every layer l: dst_k[l][dst] = src_k[l][src] and the
+    same for V, byte for byte.  The two pools are different arrays, so the
+    order of the pairs does not matter unless two pairs name the same dst (a
+    caller error; the later pair wins here).  Raises IndexError when a pair
+    lies outside its pool."""
+    pairs = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+    for l in range(len(src_k)):
+        ns, nd = src_k[l].shape[0], dst_k[l].shape[0]
+        for src, dst in pairs:
+            if not (0 <= src < ns and 0 <= dst < nd):
+                raise IndexError("swap pair outside its pool")
+            dst_k[l][dst] = src_k[l][src]
+            dst_v[l][dst] = src_v[l][src]

@@ -74,6 +74,7 @@ def load():
         "pkv_paged_attention_decode_static_ws": (i32, [dp, vp, i32, i32, i32, vp, i32, vp, i32,
                                                        f32, i32, vp, vp, vp]),
         "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [dp, i32, i32, i32, i32]),
+        "pkv_swap_blocks": (i32, [dp, dp, i32, vp, i64, vp, vp]),
         "pkv_paged_attention_prefill": (i32, [dp, vp, i32, i32, i32, vp, i32, i32, vp, i32,
                                               vp, i32, f32, vp, vp, vp]),
         "pkv_paged_attention_decode_shared_prefix": (i32, [dp, vp, i32, i32, i32, vp, i32, vp,
@@ -317,4 +318,20 @@ def pkv_paged_attention_prefill(cache, q, cu_seqlens_q, max_q_len, block_tables,
         int(max_context_len), float(scale), _ptr(dev_err), _ptr(out), _stream(stream)),
         "pkv_paged_attention_prefill")
     return out
+
+
+def pkv_swap_blocks(src, dst, block_pairs, dev_err=None, stream=None):
+    """Move blocks src[l][pairs[i, 0]] -> dst[l][pairs[i, 1]] for every layer;
+    `src` / `dst` are CacheDesc lists (device or pinned host pools)."""
+    if isinstance(src, CacheDesc):
+        src, dst = [src], [dst]
+    if len(src) != len(dst):
+        raise ValueError("src and dst need one descriptor per layer")
+    a = (CacheDesc * len(src))(*src)
+    b = (CacheDesc * len(dst))(*dst)
+    _dense(block_pairs, "block_pairs")
+    if block_pairs.dtype != torch.int64:
+        raise ValueError("block_pairs must be int64 [n, 2]")
+    _check(load().pkv_swap_blocks(a, b, len(src), _ptr(block_pairs), block_pairs.numel() // 2,
+                                  _ptr(dev_err), _stream(stream)), "pkv_swap_blocks")
 

@@ -258,6 +258,26 @@ pkv_status launch_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
     return from_cuda(pkv::launch_lse_reduce(r, stream, pdl));
 }
 
+// A pointer the GPU can dereference: device memory, or host memory that is
+// pinned and mapped into the device's address space (its device address is
+// returned; with unified addressing it is the same pointer).
+bool device_reachable(const void* p, void** dev_ptr)
+{
+    cudaPointerAttributes a{};
+    if (p == nullptr || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+        a.type == cudaMemoryTypeHost) {
+        if (a.devicePointer == nullptr)
+            return false;
+        *dev_ptr = a.devicePointer;
+        return true;
+    }
+    return false;
+}
+
 pkv_status check_workspace(const WorkspaceLayout& wl, const void* workspace, size_t bytes)
 {
     if (wl.bytes == 0)
@@ -591,6 +611,67 @@ pkv_status pkv_paged_attention_prefill(const pkv_cache_desc* cache, const void* 
     p.dev_err = dev_err;
     p.out = out;
     return from_cuda(pkv::launch_prefill(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_swap_blocks(const pkv_cache_desc* src, const pkv_cache_desc* dst,
+                           int32_t num_layers, const int64_t* block_pairs, int64_t num_pairs,
+                           int32_t* dev_err, pkv_stream_t stream)
+{
+    if (src == nullptr || dst == nullptr || num_layers <= 0 || num_pairs < 0)
+        return PKV_ERR_INVALID_ARG;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        pkv_status st = check_cache(&src[l]);
+        if (st == PKV_OK)
+            st = check_cache(&dst[l]);
+        if (st != PKV_OK)
+            return st;
+        const pkv_cache_desc& a = src[l];
+        const pkv_cache_desc& b = dst[l];
+        if (a.num_kv_heads != b.num_kv_heads || a.block_size != b.block_size ||
+            a.head_dim != b.head_dim || a.cache_dtype != b.cache_dtype ||
+            a.num_blocks != src[0].num_blocks || b.num_blocks != dst[0].num_blocks ||
+            a.num_kv_heads != src[0].num_kv_heads || a.block_size != src[0].block_size ||
+            a.head_dim != src[0].head_dim || a.cache_dtype != src[0].cache_dtype)
+            return PKV_ERR_INVALID_ARG;
+    }
+    if (num_pairs == 0)
+        return PKV_OK;
+    void* pairs_dev = nullptr;
+    if (!device_reachable(block_pairs, &pairs_dev))
+        return PKV_ERR_INVALID_ARG;
+    const pkv_cache_desc& c0 = src[0];
+    const int64_t elem = c0.cache_dtype == PKV_FP8_E4M3 ? 1 : 2;
+    pkv::SwapParams p{};
+    p.src_blocks = src[0].num_blocks;
+    p.dst_blocks = dst[0].num_blocks;
+    p.block_bytes = (int64_t)c0.num_kv_heads * c0.block_size * c0.head_dim * elem;
+    p.dev_err = dev_err;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int32_t l0 = 0; l0 < num_layers; l0 += pkv::kCopyMaxLayers) {
+        const int32_t nl = num_layers - l0 < pkv::kCopyMaxLayers ? num_layers - l0
+                                                                 : pkv::kCopyMaxLayers;
+        p.num_layers = nl;
+        for (int32_t i = 0; i < nl; ++i) {
+            void* ptrs[4];
+            if (!device_reachable(src[l0 + i].k_cache, &ptrs[0]) ||
+                !device_reachable(src[l0 + i].v_cache, &ptrs[1]) ||
+                !device_reachable(dst[l0 + i].k_cache, &ptrs[2]) ||
+                !device_reachable(dst[l0 + i].v_cache, &ptrs[3]))
+                return PKV_ERR_INVALID_ARG;
+            p.src_k[i] = ptrs[0];
+            p.src_v[i] = ptrs[1];
+            p.dst_k[i] = ptrs[2];
+            p.dst_v[i] = ptrs[3];
+        }
+        for (int64_t q0 = 0; q0 < num_pairs; q0 += 65535) {
+            p.pairs = reinterpret_cast<const int64_t*>(pairs_dev) + 2 * q0;
+            p.num_pairs = num_pairs - q0 < 65535 ? num_pairs - q0 : 65535;
+            pkv_status st = from_cuda(pkv::launch_swap_blocks(p, s));
+            if (st != PKV_OK)
+                return st;
+        }
+    }
+    return PKV_OK;
 }
 
 }  // extern "C"

@@ -137,6 +137,23 @@ struct CopyParams {
     int32_t* dev_err;
 };
 
+// Block swap between two pools (device cache, host memory), per layer.
+struct SwapParams {
+    const void* src_k[kCopyMaxLayers];
+    const void* src_v[kCopyMaxLayers];
+    void* dst_k[kCopyMaxLayers];
+    void* dst_v[kCopyMaxLayers];
+    int32_t num_layers;
+    int64_t src_blocks;
+    int64_t dst_blocks;
+    int64_t block_bytes;
+    const int64_t* pairs;          // [num_pairs][2]: src block, dst block
+    int64_t num_pairs;
+    int32_t* dev_err;
+};
+
+cudaError_t launch_swap_blocks(const SwapParams& p, cudaStream_t stream);
+
 // Each returns cudaSuccess, or cudaErrorNotSupported for a shape without a kernel.
 cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_stream(const DecodeParams& p, bool mma, cudaStream_t stream);

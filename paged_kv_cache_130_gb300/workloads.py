@@ -424,6 +424,65 @@ PREFILL_WORKLOADS = {
 }
 
 
+@dataclass
+class SwapWorkload:
+    """Pre-emption by swapping: the blocks of the `swapped` sequences of a
+    decode batch leave the device pool for pinned host memory, every layer,
+    and come back into free device blocks (「KV 缓存与分页注意力」 §09)."""
+    name: str
+    num_layers: int
+    num_blocks: int             # device pool per layer
+    host_blocks: int            # host pool per layer
+    num_kv_heads: int
+    block_size: int
+    head_dim: int
+    cache_dtype: int
+    out_pairs: np.ndarray       # int64 [n, 2]: device block -> host block
+    in_pairs: np.ndarray        # int64 [n, 2]: host block -> device block
+    swapped_seqs: np.ndarray
+    cu_seqlens_q: np.ndarray = None
+
+    @property
+    def block_bytes(self):
+        return self.num_kv_heads * self.block_size * self.head_dim * (1 if self.cache_dtype == E4M3
+                                                                       else 2)
+
+    def swap_bytes(self):
+        """Bytes one swap-out plus one swap-in move (each byte counted once):
+        K and V of every pair and layer, both directions."""
+        n = len(self.out_pairs) + len(self.in_pairs)
+        return 2 * n * self.num_layers * self.block_bytes
+
+
+def swap_opt13b_f16(seed=2, swapped=8, num_layers=40):
+    """The OPT-13B decode batch (40 layers): its `swapped` longest sequences are
+    swapped out and back in to the pool's free blocks."""
+    w = opt13b_f16(seed=seed)
+    order = np.argsort(-w.context_lens, kind="stable")[:swapped]
+    blocks = []
+    for s in order:
+        n = (int(w.context_lens[s]) + w.block_size - 1) // w.block_size
+        blocks.extend(int(b) for b in w.block_tables[s, :n])
+    blocks = np.array(blocks, np.int64)
+    used = set(int(b) for row, c in zip(w.block_tables, w.context_lens)
+               for b in row[:(int(c) + w.block_size - 1) // w.block_size])
+    free = np.array([b for b in range(w.num_blocks) if b not in used], np.int64)
+    extra = len(blocks) - len(free)
+    num_blocks = w.num_blocks + max(0, extra)
+    if extra > 0:
+        free = np.concatenate([free, np.arange(w.num_blocks, num_blocks)])
+    host = np.arange(len(blocks), dtype=np.int64)
+    dest = _rng(seed, 11).permutation(free)[:len(blocks)]
+    return SwapWorkload(name="swap_opt13b_f16", num_layers=num_layers, num_blocks=num_blocks,
+                        host_blocks=len(blocks), num_kv_heads=w.num_kv_heads,
+                        block_size=w.block_size, head_dim=w.head_dim, cache_dtype=F16,
+                        out_pairs=np.stack([blocks, host], 1),
+                        in_pairs=np.stack([host, dest], 1), swapped_seqs=order)
+
+
+SWAP_WORKLOADS = {"swap_opt13b_f16": swap_opt13b_f16}
+
+
 WORKLOADS = {
     "tiny_f16": tiny_f16,
     "opt13b_f16": opt13b_f16,
@@ -434,6 +493,8 @@ WORKLOADS = {
 
 
 def make(name, **kw):
+    if name in SWAP_WORKLOADS:
+        return SWAP_WORKLOADS[name](**kw)
     if name in PREFILL_WORKLOADS:
         return PREFILL_WORKLOADS[name](**kw)
     return WORKLOADS[name](**kw)

@@ -149,3 +149,19 @@ def test_shared_prefix_host_checks(lib):
     assert _shared(lib, d, mgs=0) == B.PKV_ERR_INVALID_ARG
     assert _shared(lib, d) == B.PKV_ERR_WORKSPACE              # the prefix needs partials
     assert _shared(lib, d, S=0) == B.PKV_OK
+
+
+def test_swap_host_checks(lib):
+    d = _desc()
+    arr = (B.CacheDesc * 1)(d)
+    other = (B.CacheDesc * 1)(_desc(head_dim=64))
+    assert lib.pkv_swap_blocks(None, arr, 1, ctypes.c_void_p(0x1000), 1, None, None) == \
+        B.PKV_ERR_INVALID_ARG
+    assert lib.pkv_swap_blocks(arr, arr, 0, ctypes.c_void_p(0x1000), 1, None, None) == \
+        B.PKV_ERR_INVALID_ARG
+    assert lib.pkv_swap_blocks(arr, other, 1, ctypes.c_void_p(0x1000), 1, None, None) == \
+        B.PKV_ERR_INVALID_ARG                                            # shapes differ
+    assert lib.pkv_swap_blocks(arr, arr, 1, None, 0, None, None) == B.PKV_OK
+    # a pointer CUDA does not know is refused before any launch
+    assert lib.pkv_swap_blocks(arr, arr, 1, ctypes.c_void_p(0x1000), 2, None, None) == \
+        B.PKV_ERR_INVALID_ARG
