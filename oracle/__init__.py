@@ -270,3 +270,29 @@ def swap_blocks(src_k, src_v, dst_k, dst_v, pairs):
                 raise IndexError("swap pair outside its pool")
             dst_k[l][dst] = src_k[l][src]
             dst_v[l][dst] = src_v[l][src]
+
+
+def block_hashes(token_ids, cu_seqlens, block_size, parent_hashes=None):
+    """Content hashes of every full block, chained over the blocks before it.
+
+    Prefix caching gives each full block a hash of its tokens and of all the
+    content in front of it, so that equal prompt openings map to the same
+    blocks (「KV 缓存与分页注意力」 §11; 「KV Cache从原理到实战」 §4.2).  Here
+    h_i = SHA-256(h_{i-1} || tokens of block i as little-endian int32), with
+    h_{-1} = parent_hashes[s] (32 zero bytes when absent); a partial last block
+    has no hash.  Returns a list, per sequence, of 32-byte digests."""
+    import hashlib
+    toks = np.asarray(token_ids, dtype=np.int32)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    out = []
+    for s in range(len(cu) - 1):
+        seq = toks[cu[s]:cu[s + 1]]
+        h = bytes(32) if parent_hashes is None else bytes(np.asarray(parent_hashes[s],
+                                                                     np.uint8))
+        hs = []
+        for b in range(len(seq) // block_size):
+            msg = h + seq[b * block_size:(b + 1) * block_size].astype("<i4").tobytes()
+            h = hashlib.sha256(msg).digest()
+            hs.append(h)
+        out.append(hs)
+    return out
