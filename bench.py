@@ -967,6 +967,158 @@ def run_gpu_swap(args, w):
     return line if rank == 0 else None
 
 
+# ------------------------------------------------------------------ hash arm
+
+HASH_METRIC = "prefix-cache block hashing GB/s (token bytes through chained SHA-256)"
+# integer operations of one SHA-256 compression: 64 rounds of ~22 and 48
+# message-schedule steps of ~12 (a rotate counts as one funnel shift)
+SHA256_OPS = 64 * 22 + 48 * 12
+
+
+def hash_alu_peak(w, sm_mhz=2070.0):
+    """Token GB/s if every INT32 lane of the GPU ran compressions: 152 SMs x
+    128 lanes x clock, / the operations of one block, x its token bytes."""
+    nch = (4 * (8 + w.block_size) + 9 + 63) // 64
+    ops = 152 * 128 * sm_mhz * 1e6
+    return ops / (nch * SHA256_OPS) * 4 * w.block_size / 1e9
+
+
+def hash_oracle_sample(w, seqs):
+    import oracle
+    cu = w.cu_seqlens.astype(np.int64)
+    toks = w.token_ids[cu[seqs[0]]:cu[seqs[-1] + 1]]
+    sub = np.concatenate([[0], np.cumsum(np.diff(cu)[seqs])])
+    t0 = time.perf_counter()
+    oracle.block_hashes(toks, sub, w.block_size)
+    t = time.perf_counter() - t0
+    full = int((np.diff(sub) // w.block_size).sum())
+    return t, 4 * w.block_size * full
+
+
+def hash_config(w):
+    return {"workload": w.name, "num_seqs": w.num_seqs, "block_size": w.block_size,
+            "tokens": int(len(w.token_ids)), "full_blocks": w.full_blocks(),
+            "hash": "SHA-256(parent hash || token ids as little-endian int32)",
+            "l2": "token ids (%.0f MB) are read once" % (len(w.token_ids) * 4 / 1e6),
+            "parallelism": "replicas"}
+
+
+def run_reference_hash(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    seqs = np.arange(min(w.num_seqs, 256))
+    for _ in range(args.warmup):
+        hash_oracle_sample(w, seqs)
+    tt, bb = 0.0, 0
+    for _ in range(args.steps):
+        t, b = hash_oracle_sample(w, seqs)
+        tt += t
+        bb += b
+    v = bb / tt / 1e9
+    return {"metric": HASH_METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic", "impl": "reference", "config": hash_config(w),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "%d of %d sequences per step" % (len(seqs), w.num_seqs)},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_gpu_hash(args, w):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_cache_130_gb300 import binding as B
+    from paged_kv_cache_130_gb300 import build as pkv_build
+
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+    pkv_build.build()
+    B.load()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    toks = torch.from_numpy(w.token_ids).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    full = np.diff(w.cu_seqlens.astype(np.int64)) // w.block_size
+    offs = torch.from_numpy(np.cumsum(full) - full).to(dev)
+    nblk = w.full_blocks()
+    hashes = torch.empty((nblk, 32), dtype=torch.uint8, device=dev)
+
+    def run():
+        B.pkv_block_hashes(toks, cu, w.block_size, block_offsets=offs, hashes=hashes)
+
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    t = slowest([sum(a.elapsed_time(b) for a, b in evs) / 1e3], dev)[0]
+    nbytes = w.hashed_token_bytes()
+    value = whole_job_rate(nbytes * args.steps, t, world) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        ht = torch.from_numpy(w.token_ids).pin_memory()
+        hcu = torch.from_numpy(w.cu_seqlens).pin_memory()
+        hoff = offs.cpu().pin_memory()
+        hh = torch.empty(hashes.shape, dtype=torch.uint8).pin_memory()
+        ms = []
+        for i in range(args.steps + args.warmup):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            toks.copy_(ht, non_blocking=True)
+            cu.copy_(hcu, non_blocking=True)
+            offs.copy_(hoff, non_blocking=True)
+            run()
+            hh.copy_(hashes, non_blocking=True)
+            b.record()
+            b.synchronize()
+            if i >= args.warmup:
+                ms.append(a.elapsed_time(b))
+        e2e_s = slowest([sum(ms) / 1e3], dev)[0]
+        e2e = {"value": whole_job_rate(nbytes * args.steps, e2e_s, world) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(4 * (len(w.token_ids) + len(w.cu_seqlens))
+                                         + 8 * w.num_seqs),
+               "d2h_bytes_per_step": int(32 * nblk), "ms_per_step": e2e_s * 1e3 / args.steps}
+    peak = hash_alu_peak(w)
+    line = {"metric": HASH_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic", "config": hash_config(w),
+            "roofline": {"bound": "alu", "achieved": value, "peak": peak, "unit": "GB/s",
+                         "frac": value / peak, "traffic": None,
+                         "kernel": "block_hash_kernel (pkv_block_hashes)",
+                         "peak_source": "derived: 152 SMs x 128 INT32 lanes x 2070 MHz / "
+                                        "%d ops per SHA-256 compression" % SHA256_OPS},
+            "e2e": e2e, "gpu_launches": args.steps, "clocks": clk}
+    if rank == 0 and not args.no_cpu_baseline:
+        tt, bb = hash_oracle_sample(w, np.arange(min(w.num_seqs, 256)))
+        line["cpu_baseline"] = {"value": bb / tt / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": "256 of %d sequences" % w.num_seqs}
+    return line if rank == 0 else None
+
+
 def main(argv=None):
     args = parse_args(argv)
     from paged_kv_cache_130_gb300 import workloads as W
@@ -974,6 +1126,11 @@ def main(argv=None):
     if args.impl == "reference" and rank != 0:
         return 0
     w = W.make(args.workload)
+    if isinstance(w, W.HashWorkload):
+        line = (run_reference_hash if args.impl == "reference" else run_gpu_hash)(args, w)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
     if isinstance(w, W.SwapWorkload):
         line = (run_reference_swap if args.impl == "reference" else run_gpu_swap)(args, w)
         if line is not None:

@@ -166,6 +166,34 @@ pkv_status pkv_swap_blocks(const pkv_cache_desc* src, const pkv_cache_desc* dst,
                            int32_t* dev_err, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Block hashes for prefix caching -- every full block gets a hash of its
+ * tokens and of all the content in front of it, so that requests with the same
+ * opening find the same blocks (「KV 缓存与分页注意力」 §11; 「KV Cache从原理到实战」
+ * §4.2).  The hash function is this library's choice (the pages name none):
+ *   h_i = SHA-256(h_{i-1} || token ids of block i as little-endian int32)
+ * (FIPS 180-4), with h_{-1} = parent_hashes[s] or 32 zero bytes.  A partial
+ * last block gets no hash.
+ *
+ * token_ids      device int32 [total_tokens]; sequence s owns
+ *                [cu_seqlens[s], cu_seqlens[s + 1]).
+ * cu_seqlens     device int32 [num_seqs + 1], ascending.
+ * parent_hashes  device [num_seqs][32] bytes (16-byte aligned) continuing
+ *                earlier chains, or NULL.
+ * block_offsets  device int64 [num_seqs]: sequence s writes its k-th block
+ *                hash to hashes[block_offsets[s] + k].
+ * hashes         device [total_blocks][32] bytes (16-byte aligned), digests
+ *                in the standard's big-endian byte order.
+ * Device checks: bad cu_seqlens or a sequence whose hashes would pass
+ * total_blocks -> PKV_DEVERR_CONTEXT, that sequence writes nothing.
+ * One thread per sequence (the chain is sequential); one launch.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens,
+                            int32_t num_seqs, int64_t total_tokens, int32_t block_size,
+                            const uint8_t* parent_hashes, const int64_t* block_offsets,
+                            int64_t total_blocks, uint8_t* hashes, int32_t* dev_err,
+                            pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Decode attention -- one query token per sequence attends over its whole
  * cached context, which the kernel reads block by block through the table.
  *   「KV 缓存与分页注意力」 §02 and §07; grouped heads: §11.

@@ -75,6 +75,7 @@ def load():
                                                        f32, i32, vp, vp, vp]),
         "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [dp, i32, i32, i32, i32]),
         "pkv_swap_blocks": (i32, [dp, dp, i32, vp, i64, vp, vp]),
+        "pkv_block_hashes": (i32, [vp, vp, i32, i64, i32, vp, vp, i64, vp, vp, vp]),
         "pkv_paged_attention_prefill": (i32, [dp, vp, i32, i32, i32, vp, i32, i32, vp, i32,
                                               vp, i32, f32, vp, vp, vp]),
         "pkv_paged_attention_decode_shared_prefix": (i32, [dp, vp, i32, i32, i32, vp, i32, vp,
@@ -334,4 +335,35 @@ def pkv_swap_blocks(src, dst, block_pairs, dev_err=None, stream=None):
         raise ValueError("block_pairs must be int64 [n, 2]")
     _check(load().pkv_swap_blocks(a, b, len(src), _ptr(block_pairs), block_pairs.numel() // 2,
                                   _ptr(dev_err), _stream(stream)), "pkv_swap_blocks")
+
+
+def pkv_block_hashes(token_ids, cu_seqlens, block_size, block_offsets=None, parent_hashes=None,
+                     hashes=None, dev_err=None, stream=None):
+    """Chained SHA-256 of every full block; returns uint8 [total_blocks, 32].
+    `block_offsets` (int64 [num_seqs]) defaults to the running count of full
+    blocks, which needs the lengths on the host (one device-to-host copy)."""
+    _dense(token_ids, "token_ids")
+    _dense(cu_seqlens, "cu_seqlens")
+    if token_ids.dtype != torch.int32 or cu_seqlens.dtype != torch.int32:
+        raise ValueError("token_ids and cu_seqlens must be int32")
+    num_seqs = cu_seqlens.numel() - 1
+    if block_offsets is None:
+        full = torch.diff(cu_seqlens.to(torch.int64)) // block_size
+        block_offsets = torch.cumsum(full, 0) - full
+        total_blocks = int(full.sum().item())
+    else:
+        _dense(block_offsets, "block_offsets")
+        total_blocks = hashes.shape[0] if hashes is not None else None
+        if total_blocks is None:
+            raise ValueError("pass `hashes` together with `block_offsets`")
+    if hashes is None:
+        hashes = torch.empty((max(total_blocks, 1), 32), dtype=torch.uint8,
+                             device=token_ids.device)
+    if parent_hashes is not None:
+        _dense(parent_hashes, "parent_hashes")
+    _check(load().pkv_block_hashes(_ptr(token_ids), _ptr(cu_seqlens), num_seqs,
+                                   token_ids.numel(), int(block_size), _ptr(parent_hashes),
+                                   _ptr(block_offsets), total_blocks, _ptr(hashes), _ptr(dev_err),
+                                   _stream(stream)), "pkv_block_hashes")
+    return hashes[:total_blocks]
 

@@ -674,4 +674,35 @@ pkv_status pkv_swap_blocks(const pkv_cache_desc* src, const pkv_cache_desc* dst,
     return PKV_OK;
 }
 
+pkv_status pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens,
+                            int32_t num_seqs, int64_t total_tokens, int32_t block_size,
+                            const uint8_t* parent_hashes, const int64_t* block_offsets,
+                            int64_t total_blocks, uint8_t* hashes, int32_t* dev_err,
+                            pkv_stream_t stream)
+{
+    if (num_seqs < 0 || total_tokens < 0 || total_blocks < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (block_size != 8 && block_size != 16 && block_size != 32)
+        return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0)
+        return PKV_OK;
+    if (cu_seqlens == nullptr || block_offsets == nullptr ||
+        (total_tokens > 0 && token_ids == nullptr) || (total_blocks > 0 && hashes == nullptr) ||
+        !aligned16(hashes) || !aligned16(parent_hashes))
+        return PKV_ERR_INVALID_ARG;
+    pkv::HashParams p{};
+    p.token_ids = token_ids;
+    p.cu_seqlens = cu_seqlens;
+    p.num_seqs = num_seqs;
+    p.total_tokens = total_tokens;
+    p.block_size = block_size;
+    p.parent_hashes = parent_hashes;
+    p.block_offsets = block_offsets;
+    p.total_blocks = total_blocks;
+    p.hashes = hashes;
+    p.dev_err = dev_err;
+    p.table = pkv::sha256_table();
+    return from_cuda(pkv::launch_block_hashes(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -154,6 +154,30 @@ struct SwapParams {
 
 cudaError_t launch_swap_blocks(const SwapParams& p, cudaStream_t stream);
 
+// SHA-256 constants (FIPS 180-4 §4.2.2, §5.3.3), derived on the host.
+struct Sha256Table {
+    uint32_t k[64];
+    uint32_t h0[8];
+};
+
+// Chained SHA-256 hashes of full blocks of token ids.
+struct HashParams {
+    const int32_t* token_ids;      // [total_tokens]
+    const int32_t* cu_seqlens;     // [num_seqs + 1]
+    int32_t num_seqs;
+    int64_t total_tokens;
+    int32_t block_size;
+    const uint8_t* parent_hashes;  // [num_seqs][32] or null (zeros)
+    const int64_t* block_offsets;  // [num_seqs]: index of each sequence's first hash
+    int64_t total_blocks;          // rows of `hashes`
+    uint8_t* hashes;               // [total_blocks][32]
+    int32_t* dev_err;
+    Sha256Table table;
+};
+
+cudaError_t launch_block_hashes(const HashParams& p, cudaStream_t stream);
+const Sha256Table& sha256_table();
+
 // Each returns cudaSuccess, or cudaErrorNotSupported for a shape without a kernel.
 cudaError_t launch_decode_partitions(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_stream(const DecodeParams& p, bool mma, cudaStream_t stream);

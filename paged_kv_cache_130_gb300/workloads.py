@@ -483,6 +483,40 @@ def swap_opt13b_f16(seed=2, swapped=8, num_layers=40):
 SWAP_WORKLOADS = {"swap_opt13b_f16": swap_opt13b_f16}
 
 
+@dataclass
+class HashWorkload:
+    """Prefix-cache hashing of a batch of prompts: the chained hash of every
+    full block of token ids (「KV 缓存与分页注意力」 §11)."""
+    name: str
+    block_size: int
+    token_ids: np.ndarray       # int32 [total_tokens]
+    cu_seqlens: np.ndarray      # int32 [num_seqs + 1]
+    cu_seqlens_q: np.ndarray = None
+
+    @property
+    def num_seqs(self):
+        return len(self.cu_seqlens) - 1
+
+    def full_blocks(self):
+        return int((np.diff(self.cu_seqlens.astype(np.int64)) // self.block_size).sum())
+
+    def hashed_token_bytes(self):
+        """Token bytes that enter a hash (full blocks only)."""
+        return 4 * self.block_size * self.full_blocks()
+
+
+def hash_prompts(seed=8, num_seqs=4096, lo=512, hi=2048, block_size=16, vocab=32000):
+    """4096 prompts of U[lo, hi] token ids drawn from a 32,000-entry vocabulary."""
+    r = _rng(seed, 0)
+    lens = r.integers(lo, hi, size=num_seqs, endpoint=True)
+    toks = _rng(seed, 1).integers(0, vocab, size=int(lens.sum())).astype(np.int32)
+    return HashWorkload(name="hash_prompts", block_size=block_size, token_ids=toks,
+                        cu_seqlens=np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+
+
+HASH_WORKLOADS = {"hash_prompts": hash_prompts}
+
+
 WORKLOADS = {
     "tiny_f16": tiny_f16,
     "opt13b_f16": opt13b_f16,
@@ -493,6 +527,8 @@ WORKLOADS = {
 
 
 def make(name, **kw):
+    if name in HASH_WORKLOADS:
+        return HASH_WORKLOADS[name](**kw)
     if name in SWAP_WORKLOADS:
         return SWAP_WORKLOADS[name](**kw)
     if name in PREFILL_WORKLOADS:

@@ -165,3 +165,15 @@ def test_swap_host_checks(lib):
     # a pointer CUDA does not know is refused before any launch
     assert lib.pkv_swap_blocks(arr, arr, 1, ctypes.c_void_p(0x1000), 2, None, None) == \
         B.PKV_ERR_INVALID_ARG
+
+
+def test_block_hash_host_checks(lib):
+    f = lib.pkv_block_hashes
+    p = ctypes.c_void_p
+    assert f(p(0x1000), p(0x2000), 2, 10, 12, None, p(0x3000), 1, p(0x4000), None, None) == \
+        B.PKV_ERR_UNSUPPORTED                                            # block size 12
+    assert f(p(0x1000), None, 2, 10, 16, None, p(0x3000), 1, p(0x4000), None, None) == \
+        B.PKV_ERR_INVALID_ARG
+    assert f(p(0x1000), p(0x2000), 2, 10, 16, None, p(0x3000), 1, p(0x4004), None, None) == \
+        B.PKV_ERR_INVALID_ARG                                            # misaligned output
+    assert f(None, None, 0, 0, 16, None, None, 0, None, None, None) == B.PKV_OK
