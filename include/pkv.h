@@ -358,7 +358,7 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
  * max_q_len     host upper bound of n_s (sizes the grid).
  * block_tables, context_lens, max_context_len: as for the decode.
  * Supported: F16 or BF16 caches with q of the same type, head_dim 64 or 128,
- *   block_size 8, 16 or 32, 1..64 query heads per KV head; others return
+ *   block_size 8, 16 or 32, 1..128 query heads per KV head; others return
  *   PKV_ERR_UNSUPPORTED.
  * Device checks (with dev_err): n_s above max_q_len or c, c above
  *   max_context_len or the table, bad cu_seqlens_q -> PKV_DEVERR_CONTEXT (that
