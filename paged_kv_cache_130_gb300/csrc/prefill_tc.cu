@@ -27,8 +27,11 @@
 // The epilogue reads O from tensor memory, divides by the sum and writes the
 // rows.  Every mbarrier wait is bounded; on time-out the CTA flags
 // PKV_DEVERR_TIMEOUT, skips the rest and still frees its tensor memory.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -128,6 +131,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// TMA: one box {64 elements, BS rows} of a 2-D tensor map into shared memory,
+// completing transaction bytes on an mbarrier.
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                        uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bar_expect(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp16z(uint32_t dst, const void* src, bool valid)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -169,14 +190,17 @@ struct TcSmem {
 };
 
 template <int CT, int D, int BS>
-__global__ void __launch_bounds__(kRowsTc, 2) prefill_tc_kernel(const PrefillParams p)
+__global__ void __launch_bounds__(kRowsTc, 2)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv)
 {
     using L = TcSmem<D>;
     constexpr int NCH = D / 8;                 // 16-byte chunks per row
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint32_t tmem_holder;
-    __shared__ __align__(8) uint64_t bars[2];  // S done, O done
+    __shared__ __align__(8) uint64_t bars[3];  // S done, O done, K/V landed
     __shared__ int abort_flag;
+    __shared__ uint32_t bad_rows[2];           // K, V blocks with a bad id (bit per block)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -225,8 +249,6 @@ __global__ void __launch_bounds__(kRowsTc, 2) prefill_tc_kernel(const PrefillPar
     unsigned char* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sb = s_addr(base);
     const char* qsrc = reinterpret_cast<const char*>(p.q);
-    const char* kc = reinterpret_cast<const char*>(p.k_cache);
-    const char* vc = reinterpret_cast<const char*>(p.v_cache);
     const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
 
     for (int i = tid; i < kRowsTc * NCH; i += blockDim.x) {
@@ -236,39 +258,60 @@ __global__ void __launch_bounds__(kRowsTc, 2) prefill_tc_kernel(const PrefillPar
         cp16z(sb + L::q + panel_off(r, c, kRowsTc), ok ? qsrc + row_off(r) * 2 + c * 16 : qsrc,
               ok);
     }
-    // K or V rows of tile kt -> `which` (L::k or L::v); keys past kv_end and
-    // bad block ids are zero-filled
-    auto load_tile = [&](int which, int kt) {
-        const char* src = which == L::k ? kc : vc;
+    // K or V of tile kt -> `which` (L::k or L::v) by TMA, one box per block
+    // and 64-dim panel, issued by one thread; returns the bytes to expect.
+    // Blocks past kv_end are not loaded (their keys are masked, and the V
+    // rows are cleared below); a bad block id is flagged and its rows cleared.
+    auto issue_tile = [&](int which, int kt) -> uint32_t {
+        const CUtensorMap* map = which == L::k ? &tmk : &tmv;
+        uint32_t bytes = 0;
+        uint32_t bad = 0;
+#pragma unroll
+        for (int bi = 0; bi < kKvTc / BS; ++bi) {
+            const int tok0 = kt * kKvTc + bi * BS;
+            if (tok0 >= kv_end)
+                break;
+            const int phys = __ldg(table + tok0 / BS);
+            if (phys < 0 || (int64_t)phys >= p.num_blocks) {
+                bad |= 1u << bi;
+                if (which == L::k)
+                    flag_error(p.dev_err, PKV_DEVERR_BLOCK_ID);
+                continue;
+            }
+            const int y = (phys * p.num_kv_heads + g) * BS;
+#pragma unroll
+            for (int pn = 0; pn < D / 64; ++pn)
+                tma_box(sb + which + pn * kKvTc * 128 + bi * BS * 128, map, pn * 64, y,
+                        s_addr(&bars[2]));
+            bytes += (uint32_t)(D / 64) * BS * 128;
+        }
+        bad_rows[which == L::k ? 0 : 1] = bad;
+        return bytes;
+    };
+    // clear rows [r0, 64) and the rows of bad blocks of a tile (generic
+    // stores, made visible to the tensor core by the proxy fence that follows)
+    auto clear_rows = [&](int which, int r0, uint32_t bad) {
         for (int i = tid; i < kKvTc * NCH; i += blockDim.x) {
             const int r = i / NCH;
             const int c = i % NCH;
-            const int tok = kt * kKvTc + r;
-            bool ok = tok < kv_end;
-            int64_t off = 0;
-            if (ok) {
-                const int phys = __ldg(table + tok / BS);
-                ok = phys >= 0 && (int64_t)phys < p.num_blocks;
-                if (!ok && c == 0 && which == L::k)
-                    flag_error(p.dev_err, PKV_DEVERR_BLOCK_ID);
-                off = ((((int64_t)phys * p.num_kv_heads + g) * BS + tok % BS) * D) * 2 + c * 16;
-            }
-            cp16z(sb + which + panel_off(r, c, kKvTc), ok ? src + off : src, ok);
+            if (r >= r0 || ((bad >> (r / BS)) & 1u))
+                st_v4(base + which + panel_off(r, c, kKvTc), make_uint4(0, 0, 0, 0));
         }
     };
     // Per tile kt (one K and one V buffer; two CTAs share an SM, so one's
     // softmax runs while the other's MMAs do):
-    //   wait S_kt; read it; wait P V_{kt-1} (frees V, P and O); load V_kt and
+    //   wait S_kt; read it; wait P V_{kt-1} (frees V, P and O); TMA V_kt and
     //   K_{kt+1}; softmax, P; then one thread issues O += P_kt V_kt and
     //   S_{kt+1} = Q K_{kt+1}^T.
-    load_tile(L::k, 0);
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");                 // Q
 
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&bars[0])));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&bars[1])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&bars[2])));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_flag = 0;
+        bar_expect(s_addr(&bars[2]), issue_tile(L::k, 0));
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -277,6 +320,13 @@ __global__ void __launch_bounds__(kRowsTc, 2) prefill_tc_kernel(const PrefillPar
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();                                                     // barrier init, bad_rows
+    if (!bar_wait(s_addr(&bars[2]), 0)) {
+        flag_error(p.dev_err, PKV_DEVERR_TIMEOUT);
+        abort_flag = 1;
+    }
+    if (bad_rows[0])
+        clear_rows(L::k, kKvTc, bad_rows[0]);
     async_proxy_fence();
     tc_fence_before();
     __syncthreads();
@@ -328,10 +378,14 @@ __global__ void __launch_bounds__(kRowsTc, 2) prefill_tc_kernel(const PrefillPar
             }
             tc_fence_after();
         }
-        load_tile(L::v, kt);
-        if (kt + 1 < nkv)
-            load_tile(L::k, kt + 1);           // S_kt is done with K
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (tid == 0) {                        // S_kt is done with K
+            uint32_t bytes = issue_tile(L::v, kt);
+            if (kt + 1 < nkv)
+                bytes += issue_tile(L::k, kt + 1);
+            else
+                bad_rows[0] = 0;
+            bar_expect(s_addr(&bars[2]), bytes);
+        }
 
         // causal mask only where some key passes some row's position
         if (kt * kKvTc + kKvTc - 1 > pos0) {
@@ -390,7 +444,20 @@ __global__ void __launch_bounds__(kRowsTc, 2) prefill_tc_kernel(const PrefillPar
                 st_v4(prow + kRowsTc * 128 + o, make_uint4(lo[0], lo[1], lo[2], lo[3]));
         }
         l_run = l_run * alpha + lsum;
-        asm volatile("cp.async.wait_group 0;" ::: "memory");       // V_kt, K_{kt+1}
+        if (!bar_wait(s_addr(&bars[2]), (kt + 1) & 1)) {          // V_kt, K_{kt+1}
+            flag_error(p.dev_err, PKV_DEVERR_TIMEOUT);
+            abort_flag = 1;
+        }
+        {
+            // V rows past kv_end (the last tile) and rows of bad blocks are
+            // cleared: P is 0 there, and 0 times stale bits must stay 0
+            const int vend = kv_end - kt * kKvTc;
+            const uint32_t bad_k = bad_rows[0], bad_v = bad_rows[1];
+            if (vend < kKvTc || bad_v)
+                clear_rows(L::v, vend < kKvTc ? vend : kKvTc, bad_v);
+            if (bad_k)
+                clear_rows(L::k, kKvTc, bad_k);
+        }
         async_proxy_fence();
         tc_fence_before();
         __syncthreads();
@@ -421,7 +488,6 @@ __global__ void __launch_bounds__(kRowsTc, 2) prefill_tc_kernel(const PrefillPar
         }
         tc_fence_after();
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
 
     // epilogue: O / l for this thread's row
@@ -451,6 +517,43 @@ __global__ void __launch_bounds__(kRowsTc, 2) prefill_tc_kernel(const PrefillPar
                      "r"(L::tmem_cols));
 }
 
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+EncodeTiled encoder()
+{
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(f);
+    });
+    return fn;
+}
+
+// The cache as a 2-D tensor [num_blocks * num_kv_heads * BS rows][D] of 16-bit
+// elements; boxes of 64 elements x BS rows land 128-byte swizzled.
+bool cache_map(CUtensorMap* map, const void* cache, int64_t rows, int D, int BS)
+{
+    EncodeTiled enc = encoder();
+    if (enc == nullptr || rows <= 0 || rows >= (int64_t)1 << 31)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)BS};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(cache), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int CT, int D, int BS>
 cudaError_t run_prefill_tc(const PrefillParams& p, cudaStream_t stream)
 {
@@ -476,7 +579,11 @@ cudaError_t run_prefill_tc(const PrefillParams& p, cudaStream_t stream)
         return cudaSuccess;
     if (ctas > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)ctas, kRowsTc, L::alloc, stream>>>(p);
+    const int64_t rows = p.num_blocks * p.num_kv_heads * BS;
+    CUtensorMap tmk, tmv;
+    if (!cache_map(&tmk, p.k_cache, rows, D, BS) || !cache_map(&tmv, p.v_cache, rows, D, BS))
+        return cudaErrorNotSupported;
+    kern<<<(unsigned)ctas, kRowsTc, L::alloc, stream>>>(p, tmk, tmv);
     return cudaGetLastError();
 }
 
