@@ -445,18 +445,32 @@ def run_gpu(args, w, prefill):
     dec_ms = [b.elapsed_time(c) for _, b, c in evs]
     pre_ms = [a.elapsed_time(b) for a, b, _ in evs]
 
-    # the dominant kernel alone (partition kernel), for the roofline
+    # the dominant kernel alone (partition kernel), for the roofline: `steps`
+    # launches back to back between one pair of events, so that the average
+    # launch duration excludes the graph-launch gap before each one (each
+    # launch streams inputs larger than L2; with --flush write a flush runs
+    # between launches and is timed per launch instead)
     part_ms = []
-    for i in range(args.steps):
-        maybe_flush(i)
+    if args.flush == "write":
+        for i in range(args.steps):
+            maybe_flush(i)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            replay["partitions"]()
+            b.record()
+            part_ms.append((a, b))
+        torch.cuda.synchronize()
+        part_ms = [a.elapsed_time(b) for a, b in part_ms]
+    else:
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        replay["partitions"]()
+        for i in range(args.steps):
+            replay["partitions"]()
         b.record()
-        part_ms.append((a, b))
-    torch.cuda.synchronize()
-    part_ms = [a.elapsed_time(b) for a, b in part_ms]
+        torch.cuda.synchronize()
+        part_ms = [a.elapsed_time(b) / args.steps] * args.steps
     clk = clocks.stop() if clocks else None
 
     dec_s = sum(dec_ms) / 1e3
@@ -465,45 +479,70 @@ def run_gpu(args, w, prefill):
     dec_s, step_s = slowest([dec_s, step_s], dev)
     value = whole_job_rate(dbytes * args.steps, dec_s, world) / 1e9
 
-    # end to end through the C ABI from pinned host buffers
+    # end to end through the C ABI from pinned host buffers: the step's
+    # inputs are packed into one pinned staging buffer and cross with one
+    # host-to-device copy; the output comes back with one device-to-host copy
     e2e = None
     if not args.no_e2e:
-        h_q = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(iodt).pin_memory()
-        h_k = torch.from_numpy(np.ascontiguousarray(sk).view(np.int16)).view(iodt).pin_memory()
-        h_v = torch.from_numpy(np.ascontiguousarray(sv).view(np.int16)).view(iodt).pin_memory()
-        h_slots = torch.from_numpy(w.step_slots).pin_memory()
-        h_bt = torch.from_numpy(w.block_tables).pin_memory()
-        h_cl = torch.from_numpy(w.context_lens).pin_memory()
-        h_pairs = torch.from_numpy(w.copy_pairs).pin_memory() if pairs is not None else None
-        h_out = torch.empty(out.shape, dtype=iodt).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
-        if h_pairs is not None:
-            h2d += h_pairs.numel() * 8
+        host_in = [("q", np.ascontiguousarray(w.q), iodt), ("k", np.ascontiguousarray(sk), iodt),
+                   ("v", np.ascontiguousarray(sv), iodt), ("slots", w.step_slots, torch.int64),
+                   ("bt", w.block_tables, torch.int32), ("cl", w.context_lens, torch.int32)]
+        if pairs is not None:
+            host_in.append(("pairs", w.copy_pairs, torch.int64))
         if shared:
-            h_gb = torch.from_numpy(grp_begin).pin_memory()
-            h_gp = torch.from_numpy(grp_blocks).pin_memory()
-            h2d += 4 * (h_gb.numel() + h_gp.numel())
-        d2h = h_out.numel() * h_out.element_size()
+            host_in += [("gb", grp_begin, torch.int32), ("gp", grp_blocks, torch.int32)]
+        offs, total = {}, 0
+        for name, arr, _ in host_in:
+            offs[name] = total
+            total += -(-arr.nbytes // 256) * 256
+        h_stage = torch.empty(total, dtype=torch.uint8).pin_memory()
+        d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+        views = {}
+        for name, arr, dt in host_in:
+            o, nb = offs[name], arr.nbytes
+            h_stage[o:o + nb].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8)
+                                                     .reshape(-1)))
+            views[name] = d_stage[o:o + nb].view(dt).view(arr.shape)
+        h_out = torch.empty(out.shape, dtype=iodt).pin_memory()
+        h2d, d2h = total, h_out.numel() * h_out.element_size()
+
+        def step_e2e():
+            if pairs is not None:
+                B.pkv_copy_blocks(desc, views["pairs"])
+            B.pkv_kv_append(desc, views["k"], views["v"], views["slots"])
+            if shared:
+                B.pkv_paged_attention_decode_shared_prefix(
+                    desc, views["q"], views["bt"], views["cl"], w.max_context_len, views["gb"],
+                    views["gp"], max_group, max_prefix, w.scale, partition_size=ps,
+                    workspace=workspace, out=out)
+            else:
+                B.pkv_paged_attention_decode(desc, views["q"], views["bt"], views["cl"],
+                                             w.max_context_len, w.scale, partition_size=ps,
+                                             workspace=workspace, out=out)
+
+        def e2e_once():
+            d_stage.copy_(h_stage, non_blocking=True)
+            step_e2e()
+            h_out.copy_(out, non_blocking=True)
+
+        run_e2e = e2e_once
+        if not args.no_graphs:
+            # the copies and the C-ABI calls of one step as one CUDA graph, so
+            # the host's call overhead stays out of the device timeline
+            e2e_once()
+            torch.cuda.synchronize()
+            ge = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ge, stream=stream):
+                e2e_once()
+            torch.cuda.synchronize()
+            run_e2e = ge.replay
         e2e_ms = []
         for i in range(args.steps + args.warmup):
             maybe_flush(i)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
-            q.copy_(h_q, non_blocking=True)
-            step_k.copy_(h_k, non_blocking=True)
-            step_v.copy_(h_v, non_blocking=True)
-            step_slots.copy_(h_slots, non_blocking=True)
-            bt.copy_(h_bt, non_blocking=True)
-            cl.copy_(h_cl, non_blocking=True)
-            if h_pairs is not None:
-                pairs.copy_(h_pairs, non_blocking=True)
-            if shared:
-                gb.copy_(h_gb, non_blocking=True)
-                gp.copy_(h_gp, non_blocking=True)
-            pre()
-            decode()
-            h_out.copy_(out, non_blocking=True)
+            run_e2e()
             b.record()
             b.synchronize()
             if i >= args.warmup:
@@ -536,7 +575,9 @@ def run_gpu(args, w, prefill):
     cfg["l2"] = ("decode inputs (%.0f MB of K/V per step) exceed the 129 MB L2; no flush"
                  % (w.kv_bytes() / 1e6) if args.flush == "none"
                  else "512 MiB written between steps (L2 flush)")
-    cfg["timing"] = "CUDA events around CUDA-graph replays" if not args.no_graphs \
+    cfg["timing"] = ("CUDA events around CUDA-graph replays; e2e: one graph per step of one "
+                     "pinned host-to-device staging copy, the C-ABI calls and the output's "
+                     "device-to-host copy") if not args.no_graphs \
         else "CUDA events around direct calls"
     cfg["partition_size"] = ps
     cfg["shared_prefix"] = ({"groups": int(len(grp_blocks)), "max_group": max_group,
@@ -754,8 +795,16 @@ def run_gpu_prefill(args, w, prefill):
                "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_s * 1e3 / args.steps}
 
+    # the kernel alone for the roofline: `steps` launches back to back
+    ra = torch.cuda.Event(enable_timing=True)
+    rb = torch.cuda.Event(enable_timing=True)
+    ra.record()
+    for _ in range(args.steps):
+        replay["attn"]()
+    rb.record()
+    torch.cuda.synchronize()
     peak, kind = tensor_peak()
-    achieved = flops / (attn_s / args.steps) / 1e12
+    achieved = flops / (ra.elapsed_time(rb) / 1e3 / args.steps) / 1e12
     line = {"metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3 / args.steps, "higher_is_better": True,
