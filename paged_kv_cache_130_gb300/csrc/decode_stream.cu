@@ -122,6 +122,30 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
 // One query head against one (block, KV head) tile in shared memory.
 // Lane layout: vector j of lane l holds token j*TPI + l/RV, elements
 // (l%RV)*EPV .. +EPV (the tile's own byte order: conflict-free 16-byte reads).
+// Packed fp32 pair arithmetic (two lanes of work per instruction); the
+// pairs travel as 64-bit registers inside the asm, so no address is taken.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rd;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
 template <int CT, int D, int BS>
 struct SimtTile {
     static constexpr int C = Elem<CT>::bytes;
@@ -135,15 +159,17 @@ struct SimtTile {
     // state of one item
     float m;
     float l;
-    float acc[EPV];
+    float2 acc2[EPV / 2];                        // acc[e] = acc2[e / 2].{x, y}
+
+    __device__ __forceinline__ float& acc(int e) { return e & 1 ? acc2[e >> 1].y : acc2[e >> 1].x; }
 
     __device__ __forceinline__ void reset()
     {
         m = kNegInf;
         l = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e)
-            acc[e] = 0.f;
+        for (int e = 0; e < EPV / 2; ++e)
+            acc2[e] = make_float2(0.f, 0.f);
     }
 
     // qf: this lane's EPV query values times scale * log2(e) * k_scale.
@@ -156,11 +182,11 @@ struct SimtTile {
         for (int j = 0; j < NV; ++j) {
             float kf[EPV];
             unpack_vec<CT>(ld_shared_v4(sk + (j * 32 + lane) * 16), kf);
-            float dot = 0.f;
+            float2 d2 = make_float2(0.f, 0.f);   // even and odd dims
 #pragma unroll
-            for (int e = 0; e < EPV; ++e)
-                dot = fmaf(qf[e], kf[e], dot);
-            x[j] = dot;
+            for (int e = 0; e < EPV; e += 2)
+                d2 = ffma2(make_float2(qf[e], qf[e + 1]), make_float2(kf[e], kf[e + 1]), d2);
+            x[j] = d2.x + d2.y;
         }
         // transpose-reduce the NV partial dots over the RV lanes of a row: each
         // round halves the list a lane keeps, so after log2(NV) rounds lane l
@@ -193,9 +219,10 @@ struct SimtTile {
         m = m_new;
         const float p = my_tok < t_end ? exp2f(xs - m_new) : 0.f;
         l = l * alpha + p;
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e)
-            acc[e] *= alpha;
+        for (int e = 0; e < EPV / 2; ++e)
+            acc2[e] = fmul2(acc2[e], a2);
         // P.V: the weight of token j sits in lane (row base) + j*DUP
         const int row_base = lane & ~(RV - 1);
 #pragma unroll
@@ -204,9 +231,10 @@ struct SimtTile {
             if (tok0 + j * TPI < t_end) {
                 float vf[EPV];
                 unpack_vec<CT>(ld_shared_v4(sv + (j * 32 + lane) * 16), vf);
+                const float2 p2 = make_float2(pj, pj);
 #pragma unroll
-                for (int e = 0; e < EPV; ++e)
-                    acc[e] = fmaf(pj, vf[e], acc[e]);
+                for (int e = 0; e < EPV; e += 2)
+                    acc2[e >> 1] = ffma2(p2, make_float2(vf[e], vf[e + 1]), acc2[e >> 1]);
             }
         }
     }
@@ -223,7 +251,7 @@ struct SimtTile {
         for (int off = RV; off < 32; off <<= 1)
 #pragma unroll
             for (int e = 0; e < EPV; ++e)
-                acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+                acc(e) += __shfl_xor_sync(0xffffffffu, acc(e), off);
     }
 };
 
@@ -277,7 +305,7 @@ struct StreamSmem {
 
 // One work item = one (partition, sequence, query head); CUDA-core consumer.
 template <int CT, int QT, int D, int BS, int NC>
-__global__ void __launch_bounds__((NC + 1) * 32)
+__global__ void __launch_bounds__((NC + 1) * 32, 3)
     decode_stream_kernel(const DecodeParams p, const int num_items, const int slot)
 {
     using Shape = StreamShape<CT, D, BS>;
@@ -541,7 +569,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
             if (lane < T::RV) {
 #pragma unroll
                 for (int e = 0; e < T::EPV; ++e)
-                    sm_acc[warp * D + lane * T::EPV + e] = st.acc[e];
+                    sm_acc[warp * D + lane * T::EPV + e] = st.acc(e);
             }
             if (lane == 0) {
                 sm_m[warp] = st.m;
