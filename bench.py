@@ -816,7 +816,7 @@ def run_gpu_prefill(args, w, prefill):
                         "prefill": attn_s * 1e3 / args.steps},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                         "kernel": "prefill_kernel (pkv_paged_attention_prefill)",
+                         "kernel": "prefill_ws_kernel (pkv_paged_attention_prefill)",
                          "peak_source": kind + " (MEASURED_PEAKS.json bf16_tflops, burst)"
                          if kind == "measured" else "fallback 1.9 PFLOP/s"},
             "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk}

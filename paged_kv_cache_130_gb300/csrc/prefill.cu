@@ -23,7 +23,7 @@ cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream)
         return cudaErrorNotSupported;
     if (p.num_seqs <= 0 || p.max_q_len <= 0)
         return cudaSuccess;
-    return launch_prefill_tc(p, stream);
+    return launch_prefill_ws(p, stream);
 }
 
 }  // namespace pkv
