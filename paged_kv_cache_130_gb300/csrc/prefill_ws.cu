@@ -8,7 +8,7 @@
 // One CTA = two query tiles (a, b) of 128 rows of one (sequence, KV head); a
 // row is a (token, head) pair, so the G heads of the KV head share every K/V
 // tile, and both query tiles share each 128-key K/V tile the CTA loads.  Three
-// warpgroups; the two softmax groups take 208 registers a thread, the third
+// warpgroups; the two softmax groups take 216 registers a thread, the third
 // gives its registers up (setmaxnreg) and two of its warps work:
 //   * warp 9 (load): walks the block table one tile ahead and gathers K and V
 //     tiles by TMA (one 2-D box per block and 64-dim panel, 128-byte swizzle)
@@ -49,13 +49,13 @@ using namespace tc;
 
 constexpr int kRows = 128;             // rows per query tile = tensor-memory lanes
 constexpr int kKeys = 128;             // keys per K/V tile
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 8;             // issues query tile a's products; warp 10 b's
 constexpr int kLoadWarp = 9;
 constexpr int kThreads = 384;          // three warpgroups: softmax a, softmax b, MMA + load
 // registers per thread after the split: 384 x 168 at launch =
 // 2 x 128 x kSoftmaxRegs + 128 x kOtherRegs
-constexpr int kSoftmaxRegs = 208;
-constexpr int kOtherRegs = 88;
+constexpr int kSoftmaxRegs = 216;
+constexpr int kOtherRegs = 72;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * 168, "register split");
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -66,9 +66,9 @@ struct WsLayout {
     static constexpr int QB = NP * kRows * 128;        // one query tile
     static constexpr int KVB = NP * kKeys * 128;       // one K or V tile
     static constexpr int q = 0;                        // [2][NP][128 rows][128 B]
-    static constexpr int k = q + 2 * QB;               // [ST][NP][128 keys][128 B]
-    static constexpr int v = k + ST * KVB;             // [ST][NP][128 keys][128 B]
-    static constexpr int bytes = v + ST * KVB;
+    static constexpr int slot = q + 2 * QB;            // [ST][K, V][NP][128 keys][128 B]
+    static constexpr int SLOT = 2 * KVB;               // one slot: K(j), then V(j - 1)
+    static constexpr int bytes = slot + ST * SLOT;
     static constexpr int alloc = bytes + 1024;         // room to align the base
     static constexpr uint32_t cols = 512;
 };
@@ -76,11 +76,13 @@ struct WsLayout {
 template <int ST>
 struct WsBars {
     uint64_t q_full[2];      // 128 arrivals: the group's Q rows are in shared memory
-    uint64_t s_full[2];      // commit: S_w(kt) (and every earlier product) done
+    uint64_t s_full[2];      // commit: S_w(kt) (and every earlier product of w) done
     uint64_t p_full[2];      // 128 arrivals: P_w(kt) written
-    uint64_t o_full[2];      // commit: O_w += P_w(kt) V(kt) done
-    uint64_t k_full[ST], k_empty[ST], v_full[ST], v_empty[ST];
-    uint64_t drain;          // commit: every product of the CTA done
+    uint64_t o_full[2];      // commit: the last O_w += P_w V done
+    uint64_t full[ST];       // slot j landed: K(j) and V(j - 1)
+    uint64_t empty[ST];      // one arrival per issuing warp: slot j no longer read
+    uint64_t issued[2];      // issuing thread w has queued its products of slot j
+    uint64_t drain[2];       // commit: every product issued by warp w done
 };
 
 __device__ __forceinline__ bool aborted(const int* flag)
@@ -206,12 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < ST; ++i) {
-            bar_init(s_addr(&bars.k_full[i]), 1);
-            bar_init(s_addr(&bars.k_empty[i]), 1);
-            bar_init(s_addr(&bars.v_full[i]), 1);
-            bar_init(s_addr(&bars.v_empty[i]), 1);
+            bar_init(s_addr(&bars.full[i]), 1);
+            bar_init(s_addr(&bars.empty[i]), ntok1 > 0 ? 2 : 1);
         }
-        bar_init(s_addr(&bars.drain), 1);
+        bar_init(s_addr(&bars.issued[0]), 1);
+        bar_init(s_addr(&bars.issued[1]), 1);
+        bar_init(s_addr(&bars.drain[0]), 1);
+        bar_init(s_addr(&bars.drain[1]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_flag = 0;
     }
@@ -275,10 +278,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < kKeys; ++j)
                         x[j] = kt * kKeys + j <= pos ? x[j] : kNegInf;
                 }
-                float mx = kNegInf;
+                // row max: eight independent chains of three-input maxima
+                float mc[8];
 #pragma unroll
-                for (int j = 0; j < kKeys; ++j)
-                    mx = fmaxf(mx, x[j]);
+                for (int i = 0; i < 8; ++i)
+                    mc[i] = fmaxf(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+                for (int j = 16; j < kKeys; j += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        mc[i] = fmax3(mc[i], x[j + 2 * i], x[j + 2 * i + 1]);
+                const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                                       fmaxf(mc[6], mc[7]));
                 const float m_cand = fmaxf(m_run, mx * qk);
                 const bool raise = m_cand > m_run + 8.f;
                 const float m_new = raise ? m_cand : m_run;
@@ -300,8 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 m_run = m_new;
-                const float neg_m = -m_new;
-                float lsum = 0.f;
+                const float2 qk2 = make_float2(qk, qk);
+                const float2 nm2 = make_float2(-m_new, -m_new);
+                float2 ls[4] = {};                     // four pairs of partial sums
                 // P over S, 16 keys at a time in those keys' own 16 columns:
                 // 8 columns of high parts, then 8 of low parts, column c of a
                 // part holding keys 2c (low half) and 2c + 1
@@ -311,27 +323,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         // exp2(s qk - m); a masked key (-inf) gives 0
-                        const float p0 = fast_exp2(fmaf(x[c0 + 2 * e], qk, neg_m));
-                        const float p1 = fast_exp2(fmaf(x[c0 + 2 * e + 1], qk, neg_m));
-                        lsum += p0 + p1;
-                        hi[e] = pack_rn<CT>(p0, p1);
-                        if constexpr (CT == kBF16)
-                            lo[e] = pack_rn<CT>(p0 - __uint_as_float(hi[e] << 16),
-                                                p1 - __uint_as_float(hi[e] & 0xffff0000u));
-                        else
+                        const float2 t = ffma2(make_float2(x[c0 + 2 * e], x[c0 + 2 * e + 1]), qk2, nm2);
+                        const float2 pp = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                        ls[e & 3] = fadd2(ls[e & 3], pp);
+                        hi[e] = pack_rn<CT>(pp.x, pp.y);
+                        if constexpr (CT == kBF16) {
+                            const float2 r = fsub2(pp, make_float2(__uint_as_float(hi[e] << 16),
+                                                                   __uint_as_float(hi[e] & 0xffff0000u)));
+                            lo[e] = pack_rn<CT>(r.x, r.y);
+                        } else {
                             lo[e] = 0u;
+                        }
                     }
                     tmem_st8(t_s + c0, hi);
                     if constexpr (CT == kBF16)
                         tmem_st8(t_s + c0 + 8, lo);
                 }
+                const float lsum = ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) +
+                                   ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
                 tmem_wait_st();
                 l_run = l_run * alpha + lsum;
                 tc_fence_before();
                 bar_arrive(s_addr(&bars.p_full[w]));
             }
             if (alive)
-                alive = wait_warp(s_addr(&bars.o_full[w]), (nkv - 1) & 1, &abort_flag, p.dev_err);
+                alive = wait_warp(s_addr(&bars.o_full[w]), 0, &abort_flag, p.dev_err);
             if (alive) {
                 // epilogue: O / l for this thread's row
                 tc_fence_after();
@@ -357,76 +373,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     }
-    if (warp == kMmaWarp) {
-        // ---------------- tensor-core issue (one thread) ----------------
-        if (lane == 0) {
-            const uint32_t id_s = instr_desc<CT>(kRows, kKeys, 0);
-            const uint32_t id_o = instr_desc<CT>(kRows, D, 1);
-            bool alive = wait_one(s_addr(&bars.q_full[0]), 0, &abort_flag, p.dev_err);
-            if (alive && nkv1 > 0)
-                alive = wait_one(s_addr(&bars.q_full[1]), 0, &abort_flag, p.dev_err);
-            for (int kt = 0; alive && kt <= nk; ++kt) {
-                const int ks_ = kt % ST;               // K stage of tile kt
-                const int vs_ = (kt + ST - 1) % ST;    // V stage of tile kt - 1
-                if (kt < nk && !wait_one(s_addr(&bars.k_full[ks_]), (kt / ST) & 1, &abort_flag,
-                                         p.dev_err))
-                    break;
-                if (kt > 0 && !wait_one(s_addr(&bars.v_full[vs_]), ((kt - 1) / ST) & 1,
-                                        &abort_flag, p.dev_err))
-                    break;
+    if ((warp == kMmaWarp || warp == kMmaWarp + 2) && lane == 0 &&
+        (warp == kMmaWarp || ntok1 > 0)) {
+        // ---------------- tensor-core issue for query tile w (one thread) ----------------
+        // Each query tile has its own issuing thread; they take turns by slot
+        // (a's P V of slot j, b's, a's of slot j + 1, ...; each thread's S
+        // follows its P V and may mix with the other's next P V), so that one
+        // tile's softmax runs while the tensor core runs the other tile's
+        // products, and each thread's barrier waits overlap the other's
+        // queued products.
+        const int w = warp == kMmaWarp ? 0 : 1;
+        const int nkv = w ? nkv1 : nkv0;
+        const uint32_t id_s = instr_desc<CT>(kRows, kKeys, 0);
+        const uint32_t id_o = instr_desc<CT>(kRows, D, 1);
+        // descriptor halves: every K step only adds (bytes >> 4) to a low half
+        constexpr uint32_t hi1k = desc_hi(1024);
+        const uint32_t q_lo = desc_lo(sb + L::q + w * L::QB, 16);
+        const uint32_t k_lo = desc_lo(sb + L::slot, 16);
+        const uint32_t v_lo = desc_lo(sb + L::slot + L::KVB, kKeys * 128);
+        const uint32_t s_col = tmem + 128u * w;
+        const uint32_t o_col = tmem + 256u + (uint32_t)D * w;
+        bool alive = wait_one(s_addr(&bars.q_full[w]), 0, &abort_flag, p.dev_err);
+        // slot j: O_w += P_w(j-1) V(j-1), then S_w(j) = Q_w K(j)^T (the S_w
+        // columns P_w(j-1) occupied are written after the product read them:
+        // one thread's tensor-core operations run in issue order)
+        for (int j = 0; alive && j <= nk; ++j) {
+            const uint32_t sl = (uint32_t)((j % ST) * L::SLOT >> 4);
+            if (!wait_one(s_addr(&bars.full[j % ST]), (j / ST) & 1, &abort_flag, p.dev_err))
+                break;
+            const bool pv = j > 0 && j <= nkv;
+            if (pv && !wait_one(s_addr(&bars.p_full[w]), (j - 1) & 1, &abort_flag, p.dev_err))
+                break;
+            // the other thread's turn first (its P V of this slot for b, of the
+            // slot before for a)
+            if (w == 1 ? !wait_one(s_addr(&bars.issued[0]), j & 1, &abort_flag, p.dev_err)
+                       : (ntok1 > 0 && j > 0 &&
+                          !wait_one(s_addr(&bars.issued[1]), (j - 1) & 1, &abort_flag, p.dev_err)))
+                break;
+            bool used = false;
+            if (pv) {
+                tc_fence_after();
+                const uint32_t acc0 = j > 1 ? 1u : 0u;
 #pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    const int nkv = w ? nkv1 : nkv0;
-                    const uint32_t s_col = tmem + 128u * w;
-                    if (kt > 0 && kt <= nkv) {
-                        // O_w += P_w(kt-1) V(kt-1)
-                        if (!wait_one(s_addr(&bars.p_full[w]), (kt - 1) & 1, &abort_flag,
-                                      p.dev_err)) {
-                            alive = false;
-                            break;
-                        }
-                        tc_fence_after();
+                for (int ks = 0; ks < kKeys / 16; ++ks)
 #pragma unroll
-                        for (int part = 0; part < PARTS; ++part)
-#pragma unroll
-                            for (int ks = 0; ks < kKeys / 16; ++ks) {
-                                // 16 keys further along V's rows; 64-dim panels
-                                // are kKeys * 128 bytes apart
-                                const uint64_t bd = smem_desc(
-                                    sb + L::v + vs_ * L::KVB + ks * 16 * 128, kKeys * 128, 1024);
-                                umma_ts(tmem + 256u + (uint32_t)D * w,
-                                        s_col + ks * 16 + part * 8, bd, id_o,
-                                        (kt > 1 || ks > 0 || part > 0) ? 1u : 0u);
-                            }
-                        umma_commit(s_addr(&bars.o_full[w]));
-                    }
-                    if (kt < nkv) {
-                        // S_w(kt) = Q_w K(kt)^T
-                        tc_fence_after();
-#pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t koff = (uint32_t)(ks & 3) * 32;
-                            const uint64_t a = smem_desc(
-                                sb + L::q + w * L::QB + (ks >> 2) * kRows * 128 + koff, 16, 1024);
-                            const uint64_t bd = smem_desc(
-                                sb + L::k + ks_ * L::KVB + (ks >> 2) * kKeys * 128 + koff, 16,
-                                1024);
-                            umma(s_col, a, bd, id_s, ks > 0);
-                        }
-                        umma_commit(s_addr(&bars.s_full[w]));
-                    }
-                }
-                if (!alive)
-                    break;
-                if (kt < nk)
-                    umma_commit(s_addr(&bars.k_empty[ks_]));
-                if (kt > 0)
-                    umma_commit(s_addr(&bars.v_empty[vs_]));
+                    for (int part = 0; part < PARTS; ++part)
+                        // 16 keys further along V's rows; 64-dim panels are
+                        // kKeys * 128 bytes apart
+                        umma_ts_h(o_col, s_col + ks * 16 + part * 8,
+                                  v_lo + sl + (uint32_t)(ks * 16 * 128 >> 4), hi1k, id_o,
+                                  (ks > 0 || part > 0) ? 1u : acc0);
+                if (j == nkv)
+                    umma_commit(s_addr(&bars.o_full[w]));
+                used = true;
             }
-            // every product (and every commit's arrival) done before teardown
-            umma_commit(s_addr(&bars.drain));
-            bar_wait(s_addr(&bars.drain), 0);
+            // the other thread may queue its P V while this one queues S
+            bar_arrive(s_addr(&bars.issued[w]));
+            if (j < nkv) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (uint32_t)(((ks >> 2) * kRows * 128 + (ks & 3) * 32) >> 4);
+                    const uint32_t offk = (uint32_t)(((ks >> 2) * kKeys * 128 + (ks & 3) * 32) >> 4);
+                    umma_h(s_col, q_lo + off, hi1k, k_lo + sl + offk, hi1k, id_s, ks > 0 ? 1u : 0u);
+                }
+                umma_commit(s_addr(&bars.s_full[w]));
+                used = true;
+            }
+            // this thread no longer reads slot j once its products are done
+            if (used)
+                umma_commit(s_addr(&bars.empty[j % ST]));
+            else
+                bar_arrive(s_addr(&bars.empty[j % ST]));
         }
+        // every product (and every commit's arrival) done before teardown
+        umma_commit(s_addr(&bars.drain[w]));
+        bar_wait(s_addr(&bars.drain[w]), 0);
     } else if (warp == kLoadWarp) {
         // ---------------- loads (one warp) ----------------
         const int32_t* table = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
@@ -443,45 +465,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return phys;
         };
-        int issued_k = 0, issued_v = 0;
-        auto load = [&](bool is_v, int kt, int ent) -> bool {
-            const int st = kt % ST;
-            const uint32_t use = (uint32_t)(kt / ST);
-            const uint32_t full = s_addr(is_v ? &bars.v_full[st] : &bars.k_full[st]);
-            const uint32_t empty = s_addr(is_v ? &bars.v_empty[st] : &bars.k_empty[st]);
-            if (!wait_warp(empty, (use & 1) ^ 1, &abort_flag, p.dev_err))
+        int issued = 0;
+        // slot j: K(j) (j < nk) and V(j - 1) (j > 0), in one phase of full[j % ST]
+        auto load = [&](int j, int ent_k, int ent_v) -> bool {
+            const int st = j % ST;
+            const uint32_t full = s_addr(&bars.full[st]);
+            if (!wait_warp(s_addr(&bars.empty[st]), ((j / ST) & 1) ^ 1, &abort_flag, p.dev_err))
                 return false;
-            const int tok = kt * kKeys + lane * BS;
+            const int tk = j * kKeys + lane * BS;          // first key of K block `lane`
+            const int tv = tk - kKeys;                      // first key of V block `lane`
             // by TMA: every block of keys but the V block that holds the
             // context's last token (its rows past the context are not keys)
-            const bool tma = lane < NB && ent >= 0 && !(is_v && tok + BS > ctx);
+            const bool tma_k = j < nk && lane < NB && ent_k >= 0;
+            const bool tma_v = j > 0 && lane < NB && ent_v >= 0 && tv + BS <= ctx;
             // by plain stores: that block (its keys copied, the other rows
             // zeroed), V blocks past the CTA's last key (zeroed: their weights
             // are 0, and 0 x NaN would not be) and blocks with a bad id
             // (zeroed); K blocks past the last key stay as they are (masked)
-            const bool plain = lane < NB && !tma && (is_v || ent == -2);
-            const uint32_t tmask = __ballot_sync(0xffffffffu, tma);
-            uint32_t pmask = __ballot_sync(0xffffffffu, plain);
+            const bool plain_k = j < nk && lane < NB && ent_k == -2;
+            const bool plain_v = j > 0 && lane < NB && !tma_v;
+            const uint32_t nbox = __popc(__ballot_sync(0xffffffffu, tma_k)) +
+                                  __popc(__ballot_sync(0xffffffffu, tma_v));
             if (lane == 0)
-                bar_expect_only(full, (uint32_t)__popc(tmask) * (D / 64) * BS * 128);
+                bar_expect_only(full, nbox * (uint32_t)(D / 64) * BS * 128);
             __syncwarp();
-            if (tma) {
-                const uint32_t dst = sb + (is_v ? L::v : L::k) + st * L::KVB + lane * BS * 128;
-                const int y = (ent * p.num_kv_heads + g) * BS;
+            const uint32_t dst = sb + L::slot + st * L::SLOT + lane * BS * 128;
+            if (tma_k) {
+                const int y = (ent_k * p.num_kv_heads + g) * BS;
 #pragma unroll
                 for (int pn = 0; pn < D / 64; ++pn)
-                    tma_box(dst + pn * kKeys * 128, is_v ? &tmv : &tmk, pn * 64, y, full);
+                    tma_box(dst + pn * kKeys * 128, &tmk, pn * 64, y, full);
             }
-            if (pmask) {
-                unsigned char* sdst = base + (is_v ? L::v : L::k) + st * L::KVB;
-                const char* csrc = reinterpret_cast<const char*>(is_v ? p.v_cache : p.k_cache);
-                while (pmask) {
-                    const int bl = __ffs(pmask) - 1;
-                    pmask &= pmask - 1;
-                    const int bent = __shfl_sync(0xffffffffu, ent, bl);
-                    const int rem = bent >= 0 ? ctx - (kt * kKeys + bl * BS) : 0;  // rows that are keys
+            if (tma_v) {
+                const int y = (ent_v * p.num_kv_heads + g) * BS;
+#pragma unroll
+                for (int pn = 0; pn < D / 64; ++pn)
+                    tma_box(dst + L::KVB + pn * kKeys * 128, &tmv, pn * 64, y, full);
+            }
+            uint32_t pm_k = __ballot_sync(0xffffffffu, plain_k);
+            uint32_t pm_v = __ballot_sync(0xffffffffu, plain_v);
+            if (pm_k | pm_v) {
+                while (pm_k | pm_v) {
+                    const bool is_v = pm_k == 0;
+                    int bl;
+                    if (is_v) {
+                        bl = __ffs(pm_v) - 1;
+                        pm_v &= pm_v - 1;
+                    } else {
+                        bl = __ffs(pm_k) - 1;
+                        pm_k &= pm_k - 1;
+                    }
+                    const int bent = __shfl_sync(0xffffffffu, is_v ? ent_v : ent_k, bl);
+                    // rows that are keys (V: only a block below the last key
+                    // that holds the context's last token has some)
+                    const int first = (is_v ? j - 1 : j) * kKeys + bl * BS;
+                    const int rem = bent >= 0 ? ctx - first : 0;
                     const char* src =
-                        csrc + ((int64_t)max(bent, 0) * p.num_kv_heads + g) * BS * D * 2;
+                        reinterpret_cast<const char*>(is_v ? p.v_cache : p.k_cache) +
+                        ((int64_t)max(bent, 0) * p.num_kv_heads + g) * BS * D * 2;
+                    unsigned char* sdst = base + L::slot + st * L::SLOT + (is_v ? L::KVB : 0);
                     for (int i = lane; i < BS * NCH; i += 32) {
                         const int rr = i / NCH;
                         const int c = i % NCH;
@@ -495,30 +537,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 bar_arrive(full);
-            if (is_v)
-                ++issued_v;
-            else
-                ++issued_k;
+            ++issued;
             return true;
         };
-        int cur = entry(0);
-        bool alive = load(false, 0, cur);
-        for (int kt = 0; alive && kt < nk; ++kt) {
-            int nxt = -1;
-            if (kt + 1 < nk) {
-                nxt = entry(kt + 1);
-                if (!(alive = load(false, kt + 1, nxt)))
-                    break;
-            }
-            alive = load(true, kt, cur);
-            cur = nxt;
+        int prev = -1;                                     // entries of tile j - 1
+        bool alive = true;
+        for (int j = 0; alive && j <= nk; ++j) {
+            const int cur = j < nk ? entry(j) : -1;
+            alive = load(j, cur, prev);
+            prev = cur;
         }
         if (!alive) {
             // wait (bounded) for the copies still in flight
-            for (int i = max(0, issued_k - ST); i < issued_k; ++i)
-                bar_wait(s_addr(&bars.k_full[i % ST]), (i / ST) & 1);
-            for (int i = max(0, issued_v - ST); i < issued_v; ++i)
-                bar_wait(s_addr(&bars.v_full[i % ST]), (i / ST) & 1);
+            for (int i = max(0, issued - ST); i < issued; ++i)
+                bar_wait(s_addr(&bars.full[i % ST]), (i / ST) & 1);
         }
     }
 

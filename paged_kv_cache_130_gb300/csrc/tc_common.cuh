@@ -66,6 +66,38 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
                  "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// The same with the descriptors given as 32-bit halves (lo: start address and
+// leading offset, hi: stride offset, version and swizzle), so that a loop over
+// K steps only adds to the low halves.
+__device__ __forceinline__ void umma_h(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                       uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile("{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %6, 0;\n"
+                 " mov.b64 da, {%1, %2};\n mov.b64 db, {%3, %4};\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}" ::"r"(d_tmem),
+                 "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_ts_h(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n .reg .pred p;\n .reg .b64 db;\n setp.ne.b32 p, %5, 0;\n"
+                 " mov.b64 db, {%2, %3};\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}" ::"r"(d_tmem),
+                 "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
+}
+
+// Halves of a 128-byte-swizzle shared-memory descriptor (see smem_desc).
+__host__ __device__ constexpr uint32_t desc_lo(uint32_t addr, uint32_t lbo)
+{
+    return ((addr >> 4) & 0x3fffu) | (((lbo >> 4) & 0x3fffu) << 16);
+}
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo)
+{
+    return ((sbo >> 4) & 0x3fffu) | (1u << 14) | (2u << 29);
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -80,6 +112,19 @@ __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test of the same phase.
+__device__ __forceinline__ bool test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -195,6 +240,48 @@ __device__ __forceinline__ uint32_t pack_rn(float a, float b)
         asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(a), "f"(b));
     else
         asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// Two fp32 lanes per instruction (sm_100 family): a b + c, a + b, a - b.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rd;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rd;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " sub.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+// max of three (a NaN operand is ignored, as fmaxf does)
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
 
