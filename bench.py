@@ -42,23 +42,33 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch of the decode partition kernel from an ncu capture,
 # valid while the decode kernel sources hash to "src_sha" (else reported as null)
 NCU_TRAFFIC = {
-    "opt13b_f16": {"bytes_per_launch": 366103040 + 3534592, "src_sha": "3960089f22385274"},
-    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642891008 + 3133440,
-                            "src_sha": "3960089f22385274"},
+    "opt13b_f16": {"bytes_per_launch": 366100224 + 3444736, "src_sha": "11c0cb12314d6cef"},
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642875392 + 3086848,
+                            "src_sha": "11c0cb12314d6cef"},
     # prefix kernel + partition kernel of one shared-prefix decode call
     "cow_parallel_sampling_f16:shared-prefix": {
-        "bytes_per_launch": 130866944 + 2750464 + 251813888 + 3623680,
-        "src_sha": "3960089f22385274"},
+        "bytes_per_launch": 130866176 + 2874112 + 251794432 + 788992,
+        "src_sha": "11c0cb12314d6cef"},
 }
 DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_common.cuh")
+# the same for the prefill kernel (DRAM bytes of one launch)
+NCU_PREFILL_TRAFFIC = {
+    "prefill_llama2_7b_bf16": {"bytes_per_launch": 646965248 + 71444992,
+                               "src_sha": "e1f4cd0788555291"},
+}
+PREFILL_SOURCES = ("prefill_ws.cu", "tc_common.cuh", "pkv_common.cuh")
 
 
-def decode_src_sha():
+def src_sha(names):
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "paged_kv_cache_130_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def decode_src_sha():
+    return src_sha(DECODE_SOURCES)
 
 
 def shares_prefixes(w):
@@ -674,6 +684,13 @@ def run_reference_prefill(args, w, prefill):
                     "d2h_bytes_per_step": 0}}
 
 
+def prefill_traffic(w):
+    """DRAM bytes per launch from the ncu capture, while the prefill sources
+    are unchanged since (else None)."""
+    tr = NCU_PREFILL_TRAFFIC.get(w.name)
+    return tr["bytes_per_launch"] if tr and tr["src_sha"] == src_sha(PREFILL_SOURCES) else None
+
+
 def prefill_config(w):
     cfg = workload_config(w)
     cfg.update({"new_tokens": w.total_q, "max_q_len": w.max_q_len,
@@ -815,7 +832,7 @@ def run_gpu_prefill(args, w, prefill):
             "step_ms": {"append": sum(a.elapsed_time(b) for a, b, _ in evs) / args.steps,
                         "prefill": attn_s * 1e3 / args.steps},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": prefill_traffic(w),
                          "kernel": "prefill_ws_kernel (pkv_paged_attention_prefill)",
                          "peak_source": kind + " (MEASURED_PEAKS.json bf16_tflops, burst)"
                          if kind == "measured" else "fallback 1.9 PFLOP/s"},

@@ -119,7 +119,6 @@ struct PrefillParams {
 };
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
-cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);
 cudaError_t launch_prefill_ws(const PrefillParams& p, cudaStream_t stream);
 bool prefill_shape_supported(int dtype, int head_dim, int block_size, int group);
 

@@ -1,7 +1,7 @@
 // prefill.cu -- the prefill entry's shape check and launch choice.
 //
 // The prompt phase processes all new tokens of a sequence at once
-// (「KV Cache从原理到实战」 §2.3); the tensor-core kernel in prefill_tc.cu
+// (「KV Cache从原理到实战」 §2.3); the tensor-core kernel in prefill_ws.cu
 // computes it for every supported shape.
 #include <cuda_runtime.h>
 
