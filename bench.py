@@ -40,17 +40,19 @@ MODEL_LAYERS = {"opt13b_f16": 40, "llama2_70b_bf16_gqa": 80, "llama2_7b_fp8_long
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch of the decode partition kernel from an ncu capture,
-# valid while the decode kernel sources hash to "src_sha" (else reported as null)
+# valid while the decode kernel and partition-rule sources hash to "src_sha"
+# (else reported as null)
 NCU_TRAFFIC = {
-    "opt13b_f16": {"bytes_per_launch": 366100224 + 3444736, "src_sha": "11c0cb12314d6cef"},
-    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642875392 + 3086848,
-                            "src_sha": "11c0cb12314d6cef"},
+    "opt13b_f16": {"bytes_per_launch": 366129664 + 3273984, "src_sha": "a16210abd91dafd3"},
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642878464 + 3054592,
+                            "src_sha": "a16210abd91dafd3"},
     # prefix kernel + partition kernel of one shared-prefix decode call
     "cow_parallel_sampling_f16:shared-prefix": {
-        "bytes_per_launch": 130866176 + 2874112 + 251794432 + 788992,
-        "src_sha": "11c0cb12314d6cef"},
+        "bytes_per_launch": 130866432 + 2993408 + 251814144 + 835584,
+        "src_sha": "a16210abd91dafd3"},
 }
-DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_common.cuh")
+DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_common.cuh",
+                  "pkv_api.cu")
 # the same for the prefill kernel (DRAM bytes of one launch)
 NCU_PREFILL_TRAFFIC = {
     "prefill_llama2_7b_bf16": {"bytes_per_launch": 646965248 + 71444992,

@@ -225,13 +225,15 @@ pkv_status pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens,
  *   partition) the reduce kernel, chained with programmatic dependent launch.
  * ------------------------------------------------------------------------- */
 /* The partition size a decode of this shape uses: `requested` when positive,
- * else the library's choice -- one partition per context (no reduce) when the
- * batch holds at most 128 sequences, contexts at most 8192 tokens and there
- * are enough work items: num_seqs * num_heads >= 6x the SM count when every
- * query head has its own KV head or the cache is FP8, num_seqs * num_kv_heads
- * >= 3x the SM count when a 16-bit cache's KV heads serve groups of 2..16;
- * otherwise about 256 KiB of K+V per KV head and partition (1 MiB for the
- * grouped case). */
+ * else the library's choice.  With at most 128 sequences and contexts of at
+ * most 8192 tokens, work items are num_seqs * num_heads when every query head
+ * has its own KV head or the cache is FP8, num_seqs * num_kv_heads when a
+ * 16-bit cache's KV heads serve groups of 2..16; with W = 3x the SM count:
+ * items >= 2W -> one partition per context (no reduce); W <= items < 2W ->
+ * one partition per context for the first kind, and 3/4 of max_context_len
+ * (rounded up to the block size) for the grouped kind, so that only the
+ * longest contexts are cut in two.  Otherwise about 256 KiB of K+V per KV head
+ * and partition (1 MiB for the grouped case). */
 int32_t pkv_decode_partition_size(const pkv_cache_desc* cache, int32_t num_seqs,
                                   int32_t num_heads, int32_t max_context_len,
                                   int32_t requested);

@@ -107,15 +107,25 @@ int32_t resolve_partition(const pkv_cache_desc* c, int32_t num_seqs, int32_t num
     // one partition per context when there are enough items to fill the GPU:
     // both kernels take the longest contexts first, which balances this many
     // items without a split (and the reduce launch disappears).  Items are
-    // (sequence, query head) for the streaming kernel (3 resident per SM, 6
-    // per SM asked) and (sequence, KV head) for the grouped-head kernel
-    // (3 resident per SM, one full wave asked)
+    // (sequence, query head) for the streaming kernel (persistent, 3 CTAs per
+    // SM, 6 items per SM asked) and (sequence, KV head) for the grouped-head
+    // kernel (one item per CTA, 3 resident per SM).  When the grouped items
+    // fill one wave but not two, the longest contexts alone would run in the
+    // tail, so contexts longer than 3/4 of the longest are cut in two.
     const int64_t items = grouped_items ? (int64_t)num_seqs * c->num_kv_heads
                                         : (int64_t)num_seqs * num_heads;
-    const int64_t enough = (grouped_items ? 3 : 6) * (int64_t)device_sms();
-    if (num_seqs > 0 && num_seqs <= 128 && max_context_len > 0 && max_context_len <= 8192 &&
-        items >= enough)
-        return (max_context_len + c->block_size - 1) / c->block_size * c->block_size;
+    const int64_t wave = 3 * (int64_t)device_sms();
+    if (num_seqs > 0 && num_seqs <= 128 && max_context_len > 0 && max_context_len <= 8192) {
+        const int32_t bs = c->block_size;
+        if (items >= 2 * wave)
+            return (max_context_len + bs - 1) / bs * bs;
+        if (items >= wave) {
+            if (!grouped_items)
+                return (max_context_len + bs - 1) / bs * bs;
+            const int32_t cut = (3 * max_context_len + 3) / 4;
+            return (cut + bs - 1) / bs * bs;
+        }
+    }
     // K+V bytes of one KV head per partition: 256 KiB when a work item serves
     // one query head, 1 MiB when it serves a group of them
     const int64_t budget = grouped_items ? (1 << 20) : (1 << 18);

@@ -44,8 +44,11 @@ def test_partition_size_and_workspace(lib):
     d = _desc()
     # few items: split at 256 KiB of fp16 K+V (512 tokens) per KV head
     assert B.pkv_decode_partition_size(d, 4, 8, 3000, 0) == 512
-    # grouped heads, one full wave of (sequence, KV head) items: one partition
-    assert B.pkv_decode_partition_size(d, 64, 64, 3000, 0) == 3008
+    # grouped heads, between one and two waves of (sequence, KV head) items
+    # (W = 3 x 152 SMs without a GPU): the contexts above 3/4 of the longest
+    # are cut in two; two waves or more: one partition per context
+    assert B.pkv_decode_partition_size(d, 64, 64, 3000, 0) == 2256
+    assert B.pkv_decode_partition_size(d, 120, 64, 3000, 0) == 3008
     # grouped heads, fewer items: 1 MiB of K+V per partition (2048 tokens)
     assert B.pkv_decode_partition_size(d, 16, 64, 3000, 0) == 2048
     # many single-head items over short contexts: one partition per context
