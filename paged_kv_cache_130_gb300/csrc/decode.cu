@@ -89,7 +89,7 @@ __device__ __forceinline__ uint32_t reg_of(const uint4& v, int i)
 }
 
 template <int CT, int D, int BS, int NW, int NNT, bool PREFIX>
-__global__ void __launch_bounds__(NW * 32, NNT == 1 ? 3 : 2) decode_mma_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(NW * 32, NNT == 1 ? (PREFIX ? 4 : 3) : 2) decode_mma_kernel(const DecodeParams p)
 {
     constexpr bool kBf16 = (CT == kBF16);
     constexpr int NS = D / 32;          // 32-wide slices of head_dim (QK k-steps / 2)

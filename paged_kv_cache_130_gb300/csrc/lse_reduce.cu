@@ -22,6 +22,7 @@ namespace pkv {
 namespace {
 
 constexpr int kRowsPerCta = 4;
+constexpr int kFewParts = 8;           // rows with this many partials or fewer: one load round
 
 template <int QT, int D>
 __global__ void __launch_bounds__(kRowsPerCta * 32) lse_reduce_kernel(const ReduceParams p)
@@ -47,6 +48,65 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) lse_reduce_kernel(const Redu
     const int64_t base = row * p.max_partitions;
     const float* m = p.ws_m + base;
     const float* l = p.ws_l + base;
+    uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * D + lane * DPL;
+    auto store = [&](const float(&acc)[DPL], float inv_l) {
+        if constexpr (DPL == 4) {
+            const uint32_t w0 = pack2(round_to<QT>(acc[0] * inv_l), round_to<QT>(acc[1] * inv_l));
+            const uint32_t w1 = pack2(round_to<QT>(acc[2] * inv_l), round_to<QT>(acc[3] * inv_l));
+            *reinterpret_cast<uint2*>(out) = make_uint2(w0, w1);
+        } else {
+            *reinterpret_cast<uint32_t*>(out) =
+                pack2(round_to<QT>(acc[0] * inv_l), round_to<QT>(acc[1] * inv_l));
+        }
+    };
+    if (npart <= kFewParts) {
+        // every load first (m, l of partition `lane`; this lane's dims of every
+        // partial), so the merge waits for one memory round trip
+        float mi = -CUDART_INF_F;
+        float li = 0.f;
+        if (lane < npart) {
+            mi = m[lane];
+            li = l[lane];
+        }
+        float ov[kFewParts][DPL];
+        const float* o = p.ws_o + base * D + lane * DPL;
+#pragma unroll
+        for (int j = 0; j < kFewParts; ++j) {
+            if (j < npart) {
+                if constexpr (DPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(o + (int64_t)j * D);
+                    ov[j][0] = v.x, ov[j][1] = v.y, ov[j][2] = v.z, ov[j][3] = v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(o + (int64_t)j * D);
+                    ov[j][0] = v.x, ov[j][1] = v.y;
+                }
+            }
+        }
+        float M = mi;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float wl = (M == -CUDART_INF_F || mi == -CUDART_INF_F) ? 0.f : exp2f(mi - M);
+        float L = wl * li;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            L += __shfl_xor_sync(0xffffffffu, L, off);
+        float acc[DPL];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e)
+            acc[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kFewParts; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wl, j);
+            if (j < npart) {
+#pragma unroll
+                for (int e = 0; e < DPL; ++e)
+                    acc[e] = fmaf(wj, ov[j][e], acc[e]);
+            }
+        }
+        store(acc, L > 0.f ? 1.f / L : 0.f);
+        return;
+    }
     float M = -CUDART_INF_F;
     for (int i = lane; i < npart; i += 32)
         M = fmaxf(M, m[i]);
@@ -94,16 +154,7 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) lse_reduce_kernel(const Redu
             }
         }
     }
-    const float inv_l = L > 0.f ? 1.f / L : 0.f;
-    uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + row * D + lane * DPL;
-    if constexpr (DPL == 4) {
-        const uint32_t w0 = pack2(round_to<QT>(acc[0] * inv_l), round_to<QT>(acc[1] * inv_l));
-        const uint32_t w1 = pack2(round_to<QT>(acc[2] * inv_l), round_to<QT>(acc[3] * inv_l));
-        *reinterpret_cast<uint2*>(out) = make_uint2(w0, w1);
-    } else {
-        *reinterpret_cast<uint32_t*>(out) =
-            pack2(round_to<QT>(acc[0] * inv_l), round_to<QT>(acc[1] * inv_l));
-    }
+    store(acc, L > 0.f ? 1.f / L : 0.f);
 }
 
 template <int QT>
