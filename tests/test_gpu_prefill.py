@@ -98,3 +98,38 @@ def test_prefill_bad_lengths_are_flagged():
     assert torch.all(out[:20] == 0)
     ref = o.prefill_attention(np.arange(20, 50))
     H.assert_attention_close(H.out_to_double(out)[20:50], ref, "good sequence", W.F16)
+
+
+def test_prefill_grid_larger_than_the_prompts():
+    """max_q_len above every prompt: the extra work items find no rows and the
+    output is the same."""
+    w = W._prompts("prefill_wide", 33, W.BF16, 8, 2, 128, 16, [40, 300, 129], [0, 60, 7])
+    g, o = prepared(w)
+    cu = torch.from_numpy(w.cu_seqlens_q).to(g.device)
+    out = B.pkv_paged_attention_prefill(g.desc, g.q, cu, 4 * w.max_q_len + 3, g.block_tables,
+                                        g.context_lens, w.max_context_len, w.scale,
+                                        dev_err=g.dev_err)
+    torch.cuda.synchronize()
+    H.assert_attention_close(H.out_to_double(out), o.prefill_attention(), "wide grid", W.BF16)
+    assert int(g.dev_err.item()) == 0
+
+
+def test_prefill_bad_block_id_is_flagged_and_contained():
+    """A negative block id in one table: PKV_DEVERR_BLOCK_ID is raised, rows
+    whose keys all come before that block and the other sequences keep the
+    exact results, and no output is NaN (the block reads as zeros)."""
+    w = W._prompts("prefill_badblock", 34, W.F16, 4, 4, 64, 16, [300, 90], [0, 0])
+    g, o = prepared(w)
+    bt = w.block_tables.copy()
+    bad = 10                                      # keys 160..175 of sequence 0
+    bt[0, bad] = -3
+    g.block_tables.copy_(torch.from_numpy(bt))
+    out = g.prefill_attention()
+    torch.cuda.synchronize()
+    assert int(g.dev_err.item()) & B.PKV_DEVERR_BLOCK_ID
+    got = H.out_to_double(out)
+    assert not np.isnan(got).any()
+    cu = w.cu_seqlens_q
+    keep = np.r_[np.arange(cu[0], cu[0] + bad * 16), np.arange(cu[1], cu[2])]
+    H.assert_attention_close(got[keep], o.prefill_attention(keep), "rows before the bad block",
+                             W.F16)
