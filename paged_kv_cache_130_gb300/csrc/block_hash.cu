@@ -104,7 +104,18 @@ __global__ void __launch_bounds__(128) block_hash_kernel(const HashParams p)
             par[i] = 0u;
     }
     const int32_t* tok = p.token_ids + b0;
+    // the token words of block blk + 1 are read while block blk is hashed, so
+    // the chain does not wait for memory between blocks
+    uint32_t cur[BS];
+#pragma unroll
+    for (int i = 0; i < BS; ++i)
+        cur[i] = nfull > 0 ? (uint32_t)__ldg(tok + i) : 0u;
     for (int64_t blk = 0; blk < nfull; ++blk) {
+        uint32_t nxt[BS];
+        const bool more = blk + 1 < nfull;
+#pragma unroll
+        for (int i = 0; i < BS; ++i)
+            nxt[i] = more ? (uint32_t)__ldg(tok + (blk + 1) * BS + i) : 0u;
         uint32_t st[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -119,7 +130,7 @@ __global__ void __launch_bounds__(128) block_hash_kernel(const HashParams p)
                 if (j < 8)
                     v = par[j];
                 else if (j < NW)
-                    v = bswap32((uint32_t)__ldg(tok + blk * BS + (j - 8)));
+                    v = bswap32(cur[j - 8]);
                 else if (j == NW)
                     v = 0x80000000u;
                 else if (j == NCH * 16 - 1)
@@ -143,6 +154,9 @@ __global__ void __launch_bounds__(128) block_hash_kernel(const HashParams p)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             par[i] = st[i];
+#pragma unroll
+        for (int i = 0; i < BS; ++i)
+            cur[i] = nxt[i];
     }
 }
 
