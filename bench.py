@@ -56,7 +56,7 @@ DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_com
 # the same for the prefill kernel (DRAM bytes of one launch)
 NCU_PREFILL_TRAFFIC = {
     "prefill_llama2_7b_bf16": {"bytes_per_launch": 646965248 + 71444992,
-                               "src_sha": "e1f4cd0788555291"},
+                               "src_sha": "0f597fe9cf49fc30"},
 }
 PREFILL_SOURCES = ("prefill_ws.cu", "tc_common.cuh", "pkv_common.cuh")
 

@@ -32,13 +32,6 @@ __device__ __forceinline__ uint32_t panel_off(int r, int c, int rows)
     return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// Shared-memory matrix descriptor: 128-byte swizzle, version 1 (sm_100 family).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
-{
-    return (uint64_t)((addr >> 4) & 0x3fff) | ((uint64_t)((lbo >> 4) & 0x3fff) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3fff) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
 // Instruction descriptor of kind::f16 with an fp32 accumulator.
 template <int CT>
 __device__ __forceinline__ uint32_t instr_desc(int m, int n, int b_mn_major)
@@ -48,27 +41,9 @@ __device__ __forceinline__ uint32_t instr_desc(int m, int n, int b_mn_major)
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// D (tensor memory) (+)= A (shared memory) B (shared memory)
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                     uint32_t accumulate)
-{
-    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-                 "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-
-// D (tensor memory) (+)= A (tensor memory) B (shared memory)
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                        uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-                 "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
-}
-
-// The same with the descriptors given as 32-bit halves (lo: start address and
-// leading offset, hi: stride offset, version and swizzle), so that a loop over
-// K steps only adds to the low halves.
+// D (tensor memory) (+)= A (shared memory) B (shared memory), kind::f16, one
+// CTA.  The shared-memory matrix descriptors come as 32-bit halves (see
+// desc_lo / desc_hi), so that a loop over K steps only adds to the low halves.
 __device__ __forceinline__ void umma_h(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                        uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                        uint32_t accumulate)
@@ -79,6 +54,7 @@ __device__ __forceinline__ void umma_h(uint32_t d_tmem, uint32_t a_lo, uint32_t 
                  "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
 }
 
+// D (tensor memory) (+)= A (tensor memory) B (shared memory), the same way.
 __device__ __forceinline__ void umma_ts_h(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                           uint32_t b_hi, uint32_t idesc, uint32_t accumulate)
 {
@@ -88,7 +64,11 @@ __device__ __forceinline__ void umma_ts_h(uint32_t d_tmem, uint32_t a_tmem, uint
                  "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
 }
 
-// Halves of a 128-byte-swizzle shared-memory descriptor (see smem_desc).
+// Shared-memory matrix descriptor of the sm_100 family, 128-byte swizzle, as
+// two 32-bit halves.  Low: start address >> 4 (bits 0-13), leading-dimension
+// byte offset >> 4 (bits 16-29).  High: stride-dimension byte offset >> 4
+// (bits 0-13), descriptor version 1 (bit 14), swizzle mode 2 = 128-byte
+// (bits 29-31).
 __host__ __device__ constexpr uint32_t desc_lo(uint32_t addr, uint32_t lbo)
 {
     return ((addr >> 4) & 0x3fffu) | (((lbo >> 4) & 0x3fffu) << 16);
@@ -119,19 +99,6 @@ __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Non-blocking test of the same phase.
-__device__ __forceinline__ bool test_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Wait for the phase of parity `parity` of `bar`; false after kSpin rounds.
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity)
 {
@@ -149,13 +116,6 @@ __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count)
 __device__ __forceinline__ void bar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Arrive and add `bytes` to the transaction count of the current phase.
-__device__ __forceinline__ void bar_expect(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
 }
 
 // Add `bytes` to the transaction count without arriving.
