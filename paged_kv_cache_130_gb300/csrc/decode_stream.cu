@@ -313,6 +313,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
     constexpr int TILE = Shape::TILE;
     constexpr int NSTG = Shape::NSTG;
     constexpr int NCT = NC * 32;                      // consumer threads
+    // Tile t goes to consumer warp t % NC and to stage t % NSTG, and the waits
+    // on a stage's mbarrier tell its phases apart by parity only.  With NSTG a
+    // multiple of NC, tiles t and t + NSTG (consecutive uses of one stage) go
+    // to the same warp, which waits for t + NSTG only after consuming t; with
+    // any other ring size another warp could wait for t + NSTG before t's copy
+    // has landed and take that earlier phase for its own.
+    static_assert(NSTG % NC == 0, "ring stages must be a multiple of the consumer warps");
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem + L::ring;
