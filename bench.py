@@ -60,7 +60,15 @@ DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_com
 NCU_PREFILL_TRAFFIC = {
     "prefill_llama2_7b_bf16": {"bytes_per_launch": 646965248 + 71444992,
                                "src_sha": "0f597fe9cf49fc30"},
+    # one-pass capture (DRAM bytes and duration only)
+    "prefill_llama2_70b_gqa_chunked_bf16": {"bytes_per_launch": 181151488 + 29108480,
+                                            "src_sha": "0f597fe9cf49fc30"},
 }
+# the same for the block-hash kernel
+NCU_HASH_TRAFFIC = {
+    "hash_prompts": {"bytes_per_launch": 21091072 + 0, "src_sha": "3ecb8b33a5490a6c"},
+}
+HASH_SOURCES = ("block_hash.cu", "pkv_common.cuh")
 PREFILL_SOURCES = ("prefill_ws.cu", "tc_common.cuh", "pkv_common.cuh")
 
 
@@ -696,6 +704,13 @@ def prefill_traffic(w):
     return tr["bytes_per_launch"] if tr and tr["src_sha"] == src_sha(PREFILL_SOURCES) else None
 
 
+def hash_traffic(w):
+    """DRAM bytes per launch from the ncu capture, while the hash kernel's
+    sources are unchanged since (else None)."""
+    tr = NCU_HASH_TRAFFIC.get(w.name)
+    return tr["bytes_per_launch"] if tr and tr["src_sha"] == src_sha(HASH_SOURCES) else None
+
+
 def prefill_config(w):
     cfg = workload_config(w)
     cfg.update({"new_tokens": w.total_q, "max_q_len": w.max_q_len,
@@ -1178,7 +1193,7 @@ def run_gpu_hash(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
             "data": "synthetic", "config": hash_config(w),
             "roofline": {"bound": "alu", "achieved": value, "peak": peak, "unit": "GB/s",
-                         "frac": value / peak, "traffic": None,
+                         "frac": value / peak, "traffic": hash_traffic(w),
                          "kernel": "block_hash_kernel (pkv_block_hashes)",
                          "peak_source": "derived: 152 SMs x 128 INT32 lanes x 2070 MHz / "
                                         "%d ops per SHA-256 compression" % SHA256_OPS},
