@@ -59,10 +59,10 @@ DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_com
 # the same for the prefill kernel (DRAM bytes of one launch)
 NCU_PREFILL_TRAFFIC = {
     "prefill_llama2_7b_bf16": {"bytes_per_launch": 646965248 + 71444992,
-                               "src_sha": "0f597fe9cf49fc30"},
+                               "src_sha": "a635cf156331c4ca"},
     # one-pass capture (DRAM bytes and duration only)
     "prefill_llama2_70b_gqa_chunked_bf16": {"bytes_per_launch": 181151488 + 29108480,
-                                            "src_sha": "0f597fe9cf49fc30"},
+                                            "src_sha": "a635cf156331c4ca"},
 }
 # the same for the block-hash kernel
 NCU_HASH_TRAFFIC = {

@@ -9,26 +9,28 @@
 // row is a (token, head) pair, so the G heads of the KV head share every K/V
 // tile, and both query tiles share each 128-key K/V tile the CTA loads.  Three
 // warpgroups; the two softmax groups take 216 registers a thread, the third
-// gives its registers up (setmaxnreg) and two of its warps work:
-//   * warp 9 (load): walks the block table one tile ahead and gathers K and V
-//     tiles by TMA (one 2-D box per block and 64-dim panel, 128-byte swizzle)
-//     into two rings (K, V) of shared-memory stages; V blocks past the CTA's
-//     last key and blocks with a bad id are zeroed with plain stores, and
-//     the V block that holds the context's last token is copied with plain
-//     loads and its rows past the context zeroed (they may hold anything,
-//     and 0 x NaN would reach the output);
-//   * warp 8 (MMA, one thread): per K/V tile kt, for a then b,
-//     O_w += P_w(kt-1) V(kt-1) with P_w read from tensor memory, then
-//     S_w(kt) = Q_w K(kt)^T into the tensor-memory columns P_w occupied; each
-//     product commits to an mbarrier, and the commits after the last use of
-//     a stage hand it back to the load warp;
+// gives its registers up (setmaxnreg) and three of its warps work:
+//   * warp 9 (load): walks the block table one slot ahead and gathers, by TMA
+//     (one 2-D box per block and 64-dim panel, 128-byte swizzle), slot j =
+//     K(j) and V(j-1) into a two-slot shared-memory ring; V blocks past the
+//     CTA's last key and blocks with a bad id are zeroed with plain stores,
+//     and the V block that holds the context's last token is copied with
+//     plain loads and its rows past the context zeroed (they may hold
+//     anything, and 0 x NaN would reach the output);
+//   * warps 8 and 10 (one issuing thread each, for tiles a and b): per slot j,
+//     O_w += P_w(j-1) V(j-1) with P_w read from tensor memory, then
+//     S_w(j) = Q_w K(j)^T into the tensor-memory columns P_w occupied; the
+//     two threads take turns by slot, each product commits to an mbarrier,
+//     and both threads' commits after a slot's last use hand it back to the
+//     load warp;
 //   * warps 0-3 and 4-7 (softmax of a and of b, thread r = row r = tensor-
 //     memory lane r): read S_w, mask the keys past the row's position, keep a
 //     running max and sum (fp32, base 2; the max moves only when it grows by
 //     more than 2^8, so O is rarely rescaled in tensor memory) and write P_w
 //     over S_w (bf16: a high and a low part, so the weights keep ~16 bits;
-//     fp16: one part; each 16 keys in their own 16 columns).  While one group's softmax runs, the tensor core
-//     works on the other group's products.
+//     fp16: one part; each 16 keys in their own 16 columns).  While one
+//     group's softmax runs, the tensor core works on the other group's
+//     products.
 // Tensor memory (512 columns): S_a/P_a [0,128), S_b/P_b [128,256),
 // O_a [256, 256+D), O_b [256+D, 256+2D).  Every mbarrier wait is bounded; a
 // wait that gives up flags PKV_DEVERR_TIMEOUT and makes every role stop, and
@@ -49,7 +51,7 @@ using namespace tc;
 
 constexpr int kRows = 128;             // rows per query tile = tensor-memory lanes
 constexpr int kKeys = 128;             // keys per K/V tile
-constexpr int kMmaWarp = 8;             // issues query tile a's products; warp 10 b's
+constexpr int kMmaWarp = 8;            // issues query tile a's products; warp 10 b's
 constexpr int kLoadWarp = 9;
 constexpr int kThreads = 384;          // three warpgroups: softmax a, softmax b, MMA + load
 // registers per thread after the split: 384 x 168 at launch =
