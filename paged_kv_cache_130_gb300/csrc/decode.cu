@@ -88,8 +88,12 @@ __device__ __forceinline__ uint32_t reg_of(const uint4& v, int i)
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
+// Resident CTAs per SM asked of the compiler: three for one 8-head n-tile
+// (168 registers), four in prefix mode (128 registers: the 512 prefix items of
+// a parallel-sampling batch then fit one wave), two for 16 heads.
 template <int CT, int D, int BS, int NW, int NNT, bool PREFIX>
-__global__ void __launch_bounds__(NW * 32, NNT == 1 ? (PREFIX ? 4 : 3) : 2) decode_mma_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(NW * 32, NNT == 1 ? (PREFIX ? 4 : 3) : 2)
+    decode_mma_kernel(const DecodeParams p)
 {
     constexpr bool kBf16 = (CT == kBF16);
     constexpr int NS = D / 32;          // 32-wide slices of head_dim (QK k-steps / 2)
