@@ -43,16 +43,16 @@ FALLBACK_HBM_GBS = 6800.0
 # valid while the decode kernel and partition-rule sources hash to "src_sha"
 # (else reported as null)
 NCU_TRAFFIC = {
-    "opt13b_f16": {"bytes_per_launch": 366095872 + 3067904, "src_sha": "dd605a98ba9095f5"},
-    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642883840 + 2962432,
-                            "src_sha": "dd605a98ba9095f5"},
+    "opt13b_f16": {"bytes_per_launch": 366093568 + 3139328, "src_sha": "6543d3a481c9e156"},
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642883072 + 3320832,
+                            "src_sha": "6543d3a481c9e156"},
     # one-pass capture (dram bytes and duration only) on the full-size workload
-    "llama2_7b_fp8_long": {"bytes_per_launch": 2498444288 + 12621312,
-                           "src_sha": "dd605a98ba9095f5"},
+    "llama2_7b_fp8_long": {"bytes_per_launch": 2498456064 + 12672000,
+                           "src_sha": "6543d3a481c9e156"},
     # prefix kernel + partition kernel of one shared-prefix decode call
     "cow_parallel_sampling_f16:shared-prefix": {
-        "bytes_per_launch": 130873856 + 2948864 + 251793920 + 700928,
-        "src_sha": "dd605a98ba9095f5"},
+        "bytes_per_launch": 130872320 + 2930176 + 251795712 + 761600,
+        "src_sha": "6543d3a481c9e156"},
 }
 DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_common.cuh",
                   "pkv_api.cu")

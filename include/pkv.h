@@ -223,6 +223,11 @@ pkv_status pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens,
  * out           device [num_seqs][num_heads][head_dim] of q_dtype.
  * Launches: one partition kernel, then (when max_context_len exceeds one
  *   partition) the reduce kernel, chained with programmatic dependent launch.
+ *   The partition kernel of single-head (and FP8) items is itself launched
+ *   that way, so that it overlaps the end of a kv_append before it; it reads
+ *   nothing until the preceding kernel in the stream has finished.
+ * Reproducibility: the same inputs and partition size give the same output
+ *   bits on every call, whatever order the work items run in.
  * ------------------------------------------------------------------------- */
 /* The partition size a decode of this shape uses: `requested` when positive,
  * else the library's choice.  With at most 128 sequences and contexts of at

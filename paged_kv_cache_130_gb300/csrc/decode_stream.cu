@@ -352,6 +352,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
         *abort_flag = 0;
         mbar_init_fence();
     }
+    // launched with programmatic dependent launch after whatever the stream
+    // ran before: nothing is read before that work is complete (with a
+    // shared-prefix kernel before it, see wait_prior, the wait comes at the
+    // end instead)
+    if (!p.wait_prior)
+        pdl_wait_primary();
     const int ncache = min(p.num_seqs, kCtxCache);
     for (int i = threadIdx.x; i < ncache; i += blockDim.x)
         sm_ctx[i] = __ldg(p.context_lens + i);
@@ -573,14 +579,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
                     mbar_arrive(&empty[stage]);
             }
             st.finish_warp();
+            // filed by block residue k0, not by warp: the merge then adds the
+            // same partial sums in the same order whichever warp held a
+            // residue (that depends on the items the CTA took before), so a
+            // result is the same from run to run, bit for bit
             if (lane < T::RV) {
 #pragma unroll
                 for (int e = 0; e < T::EPV; ++e)
-                    sm_acc[warp * D + lane * T::EPV + e] = st.acc(e);
+                    sm_acc[k0 * D + lane * T::EPV + e] = st.acc(e);
             }
             if (lane == 0) {
-                sm_m[warp] = st.m;
-                sm_l[warp] = st.l;
+                sm_m[k0] = st.m;
+                sm_l[k0] = st.l;
             }
         }
         t += nblk;
@@ -670,7 +680,7 @@ cudaError_t run_stream(const DecodeParams& p, cudaStream_t stream)
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = p.wait_prior ? 1 : 0;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p, (int)items, slot);
 }
 

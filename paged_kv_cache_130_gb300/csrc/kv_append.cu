@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const AppendP
     const int64_t per_token = (int64_t)p.num_kv_heads * rv;
     const int64_t total = p.num_tokens * per_token;
     const int64_t pool_slots = p.num_blocks * p.block_size;
+    // a decode launched after this one may start its set-up now; it waits
+    // for this kernel's completion before it reads anything
+    pdl_launch_dependents();
 
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {

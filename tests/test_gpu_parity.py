@@ -215,6 +215,26 @@ def test_placement_does_not_change_a_bit(G):
     assert torch.equal(out1, out2)
 
 
+@pytest.mark.parametrize("name", ["opt13b_f16", "llama2_7b_fp8_long"])
+def test_repeated_decode_is_bit_identical(name):
+    """Work items go to CTAs in whatever order the device counter hands them
+    out, so the warp that holds a block residue changes from run to run; the
+    result must not."""
+    w = W.opt13b_f16(num_seqs=48) if name == "opt13b_f16" else W.llama2_7b_fp8_long(num_seqs=6)
+    g = H.GpuRun(w)
+    g.prefill()
+    g.step()
+    first = g.decode().clone()
+    for i in range(8):
+        # a decode of another batch size in between moves the counters' timing
+        if i % 2:
+            g.decode(partition_size=w.block_size * 4)
+        out = g.decode()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), first.view(torch.int16)), "run %d" % i
+    assert int(g.dev_err.item()) == 0
+
+
 def test_lse_reduce_merges_oracle_partials():
     """The reduce kernel alone, fed partials the oracle computed per range."""
     rng = np.random.default_rng(11)
