@@ -72,6 +72,15 @@ HASH_SOURCES = ("block_hash.cu", "pkv_common.cuh")
 PREFILL_SOURCES = ("prefill_ws.cu", "tc_common.cuh", "pkv_common.cuh")
 
 
+def percentiles(ms):
+    """p10 / median / p90 of per-step times (ms), nearest rank."""
+    v = sorted(ms)
+    if not v:
+        return None
+    pick = lambda q: v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))]
+    return {"p10": pick(0.1), "p50": pick(0.5), "p90": pick(0.9)}
+
+
 def src_sha(names):
     h = hashlib.sha256()
     for name in names:
@@ -617,6 +626,7 @@ def run_gpu(args, w, prefill):
                 w.num_seqs * world * args.steps / dec_s / MODEL_LAYERS.get(w.name, 1),
             "step_ms": {"copy_and_append": statistics.mean(pre_ms),
                         "decode": statistics.mean(dec_ms), "step": statistics.mean(step_ms)},
+            "decode_ms_spread": percentiles(dec_ms),
             "decode_bytes": dbytes, "unique_kv_bytes": w.unique_kv_bytes(),
             "roofline": roofline, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
@@ -851,6 +861,7 @@ def run_gpu_prefill(args, w, prefill):
             "prefill_flops": flops,
             "step_ms": {"append": sum(a.elapsed_time(b) for a, b, _ in evs) / args.steps,
                         "prefill": attn_s * 1e3 / args.steps},
+            "prefill_ms_spread": percentiles([b.elapsed_time(c) for _, b, c in evs]),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": prefill_traffic(w),
                          "kernel": "prefill_ws_kernel (pkv_paged_attention_prefill)",
