@@ -132,6 +132,29 @@ def test_decode_shapes(cdt, qdt, D, BS, G):
         assert err == 0
 
 
+@pytest.mark.parametrize("cdt,qdt,G", [(W.F16, W.F16, 1), (W.BF16, W.BF16, 8),
+                                        (W.E4M3, W.BF16, 1)])
+def test_large_batch(cdt, qdt, G):
+    """More sequences than the kernels rank by length (128) and than the
+    streaming kernel keeps context lengths for in shared memory (512): the
+    unsorted walk and the lengths read from global memory."""
+    rng = np.random.default_rng(2024 + G + 5 * cdt)
+    BS, D, Hkv = 16, 128, 2
+    ctx = list(rng.integers(1, 120, size=600))
+    ctx[3] = 0
+    ctx[599] = 1
+    ctx[77] = 400
+    kc, vc, q, bt, ctxa = _random_problem(rng, cdt, qdt, D, BS, G, Hkv, ctx)
+    ks, vs = (0.03, 0.02) if cdt == W.E4M3 else (1.0, 1.0)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    ref = oracle.paged_attention_decode(kc, vc, cdt, q, qdt, bt, ctxa, scale, ks, vs)
+    for ps in (0, 4 * BS):
+        out, err, _ = _gpu_decode(kc, vc, cdt, q, qdt, bt, ctxa, scale, ks, vs, partition_size=ps)
+        H.assert_attention_close(H.out_to_double(out), ref,
+                                 "600 sequences %s partition %d" % ((cdt, qdt, G), ps), qdt)
+        assert err == 0
+
+
 @pytest.mark.parametrize("cdt,G", [(W.F16, 1), (W.BF16, 1), (W.F16, 8), (W.BF16, 8),
                                     (W.E4M3, 1)])
 def test_single_token_context_returns_v_exactly(cdt, G):
