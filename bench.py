@@ -43,16 +43,16 @@ FALLBACK_HBM_GBS = 6800.0
 # valid while the decode kernel and partition-rule sources hash to "src_sha"
 # (else reported as null)
 NCU_TRAFFIC = {
-    "opt13b_f16": {"bytes_per_launch": 366093568 + 3139328, "src_sha": "6543d3a481c9e156"},
-    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642883072 + 3320832,
-                            "src_sha": "6543d3a481c9e156"},
+    "opt13b_f16": {"bytes_per_launch": 366095360 + 3499264, "src_sha": "dfa23bf00e5141bb"},
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642880000 + 3004160,
+                            "src_sha": "dfa23bf00e5141bb"},
     # one-pass capture (dram bytes and duration only) on the full-size workload
-    "llama2_7b_fp8_long": {"bytes_per_launch": 2498456064 + 12672000,
-                           "src_sha": "6543d3a481c9e156"},
+    "llama2_7b_fp8_long": {"bytes_per_launch": 2498218496 + 13027072,
+                           "src_sha": "dfa23bf00e5141bb"},
     # prefix kernel + partition kernel of one shared-prefix decode call
     "cow_parallel_sampling_f16:shared-prefix": {
-        "bytes_per_launch": 130872320 + 2930176 + 251795712 + 761600,
-        "src_sha": "6543d3a481c9e156"},
+        "bytes_per_launch": 130871552 + 2943488 + 251801344 + 1080832,
+        "src_sha": "dfa23bf00e5141bb"},
 }
 DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_common.cuh",
                   "pkv_api.cu")

@@ -2,7 +2,8 @@
 //
 // The grid holds as many CTAs as fit on the GPU at once.  Work items are
 // (partition, sequence, query head); the CTAs' producer warps claim them from
-// a device counter, longest contexts first.  One producer warp looks up each
+// a device counter, longest contexts first, one or (for long contexts) a few
+// consecutive partitions of one sequence and head at a time.  One producer warp looks up each
 // block through the block table (「KV 缓存与分页注意力」 §07 块表) and streams the
 // whole (block, KV head) tile of K and of V -- one contiguous run each -- into
 // a shared-memory ring with cp.async.bulk, signalling an mbarrier per stage.
@@ -17,6 +18,7 @@
 // and finishes.  There is no other wait in the kernel.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -260,6 +262,15 @@ struct SimtTile {
 constexpr int kCtxCache = 512;        // context lengths kept in shared memory
 constexpr int kSortMax = 128;         // batches up to this size are taken longest first
 constexpr int kItemQueue = 4;         // work items the producer may publish ahead
+// Work is claimed in units of unit_parts consecutive partitions of one
+// (sequence, query head): with contexts of at least kManyParts partitions,
+// as many as make up about kUnitTokens tokens (at most kMaxUnitParts), else
+// one.  A claim (a device atomic) and the block-table read behind it are
+// round trips the producer pays at the start of a unit, not of every
+// partition; units much longer than this leave the CTAs uneven at the end.
+constexpr int kManyParts = 8;
+constexpr int kUnitTokens = 2048;
+constexpr int kMaxUnitParts = 4;
 constexpr int kSchedSlots = 1024;     // launches that may be in flight at once
 
 // Dynamic work distribution.  Slot k serves one launch: [0] hands out the next
@@ -306,7 +317,8 @@ struct StreamSmem {
 // One work item = one (partition, sequence, query head); CUDA-core consumer.
 template <int CT, int QT, int D, int BS, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32, 3)
-    decode_stream_kernel(const DecodeParams p, const int num_items, const int slot)
+    decode_stream_kernel(const DecodeParams p, const int num_items, const int slot,
+                         const int unit_parts)
 {
     using Shape = StreamShape<CT, D, BS>;
     using L = StreamSmem<CT, D, BS, NC>;
@@ -393,97 +405,109 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
         int published = 0;
         bool stop = false;
         for (;;) {
-            int item = 0;
+            // one claim hands out a unit: unit_parts consecutive partitions
+            // of one (sequence, query head), streamed back to back so that
+            // the claim's and the block table's round trips are paid once
+            int unit = 0;
             if (lane == 0)
-                item = (int)atomicAdd(&g_sched[slot][0], 1u);
-            item = __shfl_sync(0xffffffffu, item, 0);
-            const bool last = item >= num_items;
-            int u = 0, s = 0, part = 0;
-            PartitionWork w{};
-            if (!last) {
-                u = item % U;
-                const int rest = item / U;
-                s = sorted ? sm_order[rest % p.num_seqs] : rest % p.num_seqs;
-                part = rest / p.num_seqs;
-                const int ctx = s < ncache ? sm_ctx[s] : __ldg(p.context_lens + s);
-                w = dec::locate_ctx(p, s, part, ctx, false);
-                if (w.idle)
-                    continue;
-            }
-            // publish the item (or the end marker)
-            const int qs = published % kItemQueue;
-            if (lane == 0) {
-                const bool ok = published < kItemQueue ||
-                                wait_bounded(&iq_empty[qs], ((published / kItemQueue) - 1) & 1,
-                                             abort_flag, p.dev_err);
-                if (ok) {
-                    items[qs] = last ? -1 : item;
-                    if (last || w.zero_out || w.zero_partial) {
-                        mbar_arrive(&iq_full[qs]);
-                    } else {
-                        // the item's query rows travel with its queue entry
-                        const int head0 = u;
-                        const uint32_t qbytes = D * 2;
-                        mbar_arrive_expect_tx(&iq_full[qs], qbytes);
-                        bulk_load(qbuf + qs * L::QSLOT,
-                                  reinterpret_cast<const char*>(p.q) +
-                                      ((int64_t)s * p.num_heads + head0) * D * 2,
-                                  qbytes, &iq_full[qs]);
-                    }
-                }
-            }
-            ++published;
-            stop = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
-            if (last || stop)
-                break;
-            if (w.zero_out || w.zero_partial)
-                continue;                              // the consumers write it
-            const int g = u / p.group;
-            const int nblk = ceil_div_i(w.t_end - w.t_begin, BS);
-            const int32_t* table =
-                p.block_tables + (int64_t)s * p.max_blocks_per_seq + w.t_begin / BS;
-            const char* kbase = reinterpret_cast<const char*>(p.k_cache) + (int64_t)g * TILE;
-            const char* vbase = reinterpret_cast<const char*>(p.v_cache) + (int64_t)g * TILE;
-            for (int c0 = 0; c0 < nblk && !stop; c0 += 32) {
-                const int n = min(32, nblk - c0);
-                const int entry = lane < n ? __ldg(table + c0 + lane) : -1;
-                for (int j = 0; j < n; ++j) {
-                    const int phys = __shfl_sync(0xffffffffu, entry, j);
-                    const uint32_t stage = t % NSTG;
-                    const uint32_t use = t / NSTG;
-                    const bool valid = phys >= 0 && (int64_t)phys < p.num_blocks;
-                    int ok = 0;
-                    if (lane == 0) {
-                        ok = use == 0 || wait_bounded(&empty[stage], (use - 1) & 1, abort_flag,
-                                                      p.dev_err);
-                        if (ok) {
-                            flags[stage] = valid ? 1 : 0;
-                            if (valid) {
-                                mbar_arrive_expect_tx(&full[stage], 2 * TILE);
-                            } else {
-                                flag_error(p.dev_err, PKV_DEVERR_BLOCK_ID);
-                                mbar_arrive(&full[stage]);
-                            }
-                            armed = t + 1;
-                        }
-                    }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (ok && valid) {
-                        unsigned char* dst = ring + stage * Shape::STAGE;
-                        const char* ksrc = kbase + (int64_t)phys * block_stride;
-                        const char* vsrc = vbase + (int64_t)phys * block_stride;
-                        if (lane == 0) {
-                            bulk_load(dst, ksrc, TILE, &full[stage]);
-                            bulk_load(dst + Shape::VOFF, vsrc, TILE, &full[stage]);
-                        }
-                    }
-                    ++t;
-                    stop = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
-                    if (stop)
+                unit = (int)atomicAdd(&g_sched[slot][0], 1u);
+            unit = __shfl_sync(0xffffffffu, unit, 0);
+            const bool last = unit >= num_items;
+            for (int sub = 0; sub < (last ? 1 : unit_parts); ++sub) {
+                int item = -1;
+                int u = 0, s = 0;
+                PartitionWork w{};
+                if (!last) {
+                    u = unit % U;
+                    const int rest = unit / U;
+                    const int rank = rest % p.num_seqs;
+                    const int part = (rest / p.num_seqs) * unit_parts + sub;
+                    if (part >= p.grid_partitions)
                         break;
+                    s = sorted ? sm_order[rank] : rank;
+                    const int ctx = s < ncache ? sm_ctx[s] : __ldg(p.context_lens + s);
+                    w = dec::locate_ctx(p, s, part, ctx, false);
+                    if (w.idle)
+                        break;                          // and so is every later part
+                    item = (part * p.num_seqs + rank) * U + u;
                 }
+                // publish the item (or the end marker)
+                const int qs = published % kItemQueue;
+                if (lane == 0) {
+                    const bool ok = published < kItemQueue ||
+                                    wait_bounded(&iq_empty[qs], ((published / kItemQueue) - 1) & 1,
+                                                 abort_flag, p.dev_err);
+                    if (ok) {
+                        items[qs] = last ? -1 : item;
+                        if (last || w.zero_out || w.zero_partial) {
+                            mbar_arrive(&iq_full[qs]);
+                        } else {
+                            // the item's query rows travel with its queue entry
+                            const int head0 = u;
+                            const uint32_t qbytes = D * 2;
+                            mbar_arrive_expect_tx(&iq_full[qs], qbytes);
+                            bulk_load(qbuf + qs * L::QSLOT,
+                                      reinterpret_cast<const char*>(p.q) +
+                                          ((int64_t)s * p.num_heads + head0) * D * 2,
+                                      qbytes, &iq_full[qs]);
+                        }
+                    }
+                }
+                ++published;
+                stop = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+                if (last || stop)
+                    break;
+                if (w.zero_out || w.zero_partial)
+                    continue;                              // the consumers write it
+                const int g = u / p.group;
+                const int nblk = ceil_div_i(w.t_end - w.t_begin, BS);
+                const int32_t* table =
+                    p.block_tables + (int64_t)s * p.max_blocks_per_seq + w.t_begin / BS;
+                const char* kbase = reinterpret_cast<const char*>(p.k_cache) + (int64_t)g * TILE;
+                const char* vbase = reinterpret_cast<const char*>(p.v_cache) + (int64_t)g * TILE;
+                for (int c0 = 0; c0 < nblk && !stop; c0 += 32) {
+                    const int n = min(32, nblk - c0);
+                    const int entry = lane < n ? __ldg(table + c0 + lane) : -1;
+                    for (int j = 0; j < n; ++j) {
+                        const int phys = __shfl_sync(0xffffffffu, entry, j);
+                        const uint32_t stage = t % NSTG;
+                        const uint32_t use = t / NSTG;
+                        const bool valid = phys >= 0 && (int64_t)phys < p.num_blocks;
+                        int ok = 0;
+                        if (lane == 0) {
+                            ok = use == 0 || wait_bounded(&empty[stage], (use - 1) & 1, abort_flag,
+                                                          p.dev_err);
+                            if (ok) {
+                                flags[stage] = valid ? 1 : 0;
+                                if (valid) {
+                                    mbar_arrive_expect_tx(&full[stage], 2 * TILE);
+                                } else {
+                                    flag_error(p.dev_err, PKV_DEVERR_BLOCK_ID);
+                                    mbar_arrive(&full[stage]);
+                                }
+                                armed = t + 1;
+                            }
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (ok && valid) {
+                            unsigned char* dst = ring + stage * Shape::STAGE;
+                            const char* ksrc = kbase + (int64_t)phys * block_stride;
+                            const char* vsrc = vbase + (int64_t)phys * block_stride;
+                            if (lane == 0) {
+                                bulk_load(dst, ksrc, TILE, &full[stage]);
+                                bulk_load(dst + Shape::VOFF, vsrc, TILE, &full[stage]);
+                            }
+                        }
+                        ++t;
+                        stop = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+                        if (stop)
+                            break;
+                    }
+                }
+                if (stop)
+                    break;
             }
-            if (stop)
+            if (last || stop)
                 break;
         }
         if (lane == 0) {
@@ -664,10 +688,16 @@ cudaError_t run_stream(const DecodeParams& p, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     const int64_t units = p.num_heads;
-    const int64_t items = (int64_t)p.grid_partitions * p.num_seqs * units;
+    // units of unit_parts consecutive partitions claimed at once
+    int unit_parts = 1;
+    if (p.grid_partitions >= kManyParts && p.partition_size > 0)
+        unit_parts = std::max(1, std::min(kMaxUnitParts, kUnitTokens / p.partition_size));
+    const int64_t items =
+        (int64_t)((p.grid_partitions + unit_parts - 1) / unit_parts) * p.num_seqs * units;
     if (items <= 0)
         return cudaSuccess;
-    if (items > 0x7fffffffLL)
+    // the ids of single partitions must fit an int as well
+    if ((int64_t)p.grid_partitions * p.num_seqs * units > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     const int64_t grid = items < (int64_t)max_ctas ? items : (int64_t)max_ctas;
     const int slot = (int)(g_launch_seq.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
@@ -681,7 +711,7 @@ cudaError_t run_stream(const DecodeParams& p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p, (int)items, slot);
+    return cudaLaunchKernelEx(&cfg, kern, p, (int)items, slot, unit_parts);
 }
 
 template <int CT, int QT, int D>
