@@ -125,6 +125,9 @@ def parse_args(argv=None):
     ap.add_argument("--shared-prefix", default="auto", choices=["auto", "off"],
                     help="auto: decode batches with forked sequences through the "
                          "shared-prefix entry point (each shared block read once per group)")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="a smaller batch of the same decode workload (profiler "
+                         "captures); the line's config names the batch")
     ap.add_argument("--flush", default="none", choices=["none", "write"],
                     help="none: the decode inputs alone exceed L2; write: also write "
                          "512 MiB between steps")
@@ -1222,7 +1225,8 @@ def main(argv=None):
     world, rank, _ = dist_env()
     if args.impl == "reference" and rank != 0:
         return 0
-    w = W.make(args.workload)
+    w = W.make(args.workload) if args.num_seqs is None else \
+        W.make(args.workload, num_seqs=args.num_seqs)
     if isinstance(w, W.HashWorkload):
         line = (run_reference_hash if args.impl == "reference" else run_gpu_hash)(args, w)
         if line is not None:
