@@ -47,3 +47,22 @@ def test_single_process_keeps_its_timings():
     import bench
     assert bench.slowest([1.0, 2.0]) == [1.0, 2.0]
     assert bench.whole_job_rate(10.0, 2.0, 1) == 5.0
+
+
+def test_percentiles_nearest_rank():
+    import bench
+    assert bench.percentiles([]) is None
+    assert bench.percentiles([3.0]) == {"p10": 3.0, "p50": 3.0, "p90": 3.0}
+    got = bench.percentiles([float(x) for x in range(10, 0, -1)])   # 10 .. 1, unsorted
+    assert got == {"p10": 2.0, "p50": 5.0, "p90": 9.0}
+
+
+def test_num_seqs_option_shrinks_the_batch():
+    import bench
+    from paged_kv_cache_130_gb300 import workloads as W
+    args = bench.parse_args(["--workload", "opt13b_f16", "--num-seqs", "4"])
+    assert args.num_seqs == 4
+    w = W.make(args.workload, num_seqs=args.num_seqs)
+    assert w.num_seqs == 4 and w.q.shape[0] == 4 and w.block_tables.shape[0] == 4
+    assert W.make(args.workload).num_seqs == 32
+    assert bench.parse_args([]).num_seqs is None
