@@ -7,7 +7,7 @@
 // followed by those of the rest of the context.
 // One warp per (sequence, head) row: lanes read the row's m and l strided,
 // reduce M and the weighted l with shuffles, then every lane accumulates its
-// D/32 output dims over the partitions with independent vector loads.
+// D/32 output dims over the partitions, many vector loads in flight at once.
 // Launched with programmatic dependent launch: the context length is read
 // before griddepcontrol.wait (it is an input, not a partial), the partials
 // after it.
@@ -107,14 +107,39 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) lse_reduce_kernel(const Redu
         store(acc, L > 0.f ? 1.f / L : 0.f);
         return;
     }
+    // More partials: lane i keeps m and l of partitions i, i + 32, ... (up to
+    // kKeptChunks of them) in registers, so M and the weighted l need one
+    // round trip; then each lane accumulates its dims over the partitions
+    // kBatch loads at a time (all issued before the first is used).
+    constexpr int kKeptChunks = 4;
+    constexpr int kBatch = 16;
+    float mr[kKeptChunks];
+    float lr[kKeptChunks];
     float M = -CUDART_INF_F;
-    for (int i = lane; i < npart; i += 32)
+#pragma unroll
+    for (int c = 0; c < kKeptChunks; ++c) {
+        const int i = lane + 32 * c;
+        mr[c] = -CUDART_INF_F;
+        lr[c] = 0.f;
+        if (i < npart) {
+            mr[c] = m[i];
+            lr[c] = l[i];
+        }
+        M = fmaxf(M, mr[c]);
+    }
+    for (int i = lane + 32 * kKeptChunks; i < npart; i += 32)
         M = fmaxf(M, m[i]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float wr[kKeptChunks];
     float L = 0.f;
-    for (int i = lane; i < npart; i += 32) {
+#pragma unroll
+    for (int c = 0; c < kKeptChunks; ++c) {
+        wr[c] = (M == -CUDART_INF_F || mr[c] == -CUDART_INF_F) ? 0.f : exp2f(mr[c] - M);
+        L += wr[c] * lr[c];
+    }
+    for (int i = lane + 32 * kKeptChunks; i < npart; i += 32) {
         const float mi = m[i];
         if (M != -CUDART_INF_F && mi != -CUDART_INF_F)
             L += exp2f(mi - M) * l[i];
@@ -128,31 +153,46 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) lse_reduce_kernel(const Redu
     for (int e = 0; e < DPL; ++e)
         acc[e] = 0.f;
     const float* o = p.ws_o + base * D + lane * DPL;
-    for (int c0 = 0; c0 < npart; c0 += 32) {
-        // weight of partition c0 + lane, then broadcast one by one
+    // partitions c0 + [0, n), weight of c0 + j held by lane j
+    auto accumulate = [&](int c0, int n, float wl) {
+        for (int j0 = 0; j0 < n; j0 += kBatch) {
+            float v[kBatch][DPL];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (j0 + k < n) {
+                    const float* oj = o + (int64_t)(c0 + j0 + k) * D;
+                    if constexpr (DPL == 4) {
+                        const float4 t = *reinterpret_cast<const float4*>(oj);
+                        v[k][0] = t.x, v[k][1] = t.y, v[k][2] = t.z, v[k][3] = t.w;
+                    } else {
+                        const float2 t = *reinterpret_cast<const float2*>(oj);
+                        v[k][0] = t.x, v[k][1] = t.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const float wj = __shfl_sync(0xffffffffu, wl, (j0 + k) & 31);
+                if (j0 + k < n) {
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e)
+                        acc[e] = fmaf(wj, v[k][e], acc[e]);
+                }
+            }
+        }
+    };
+#pragma unroll
+    for (int c = 0; c < kKeptChunks; ++c)
+        if (32 * c < npart)
+            accumulate(32 * c, min(32, npart - 32 * c), wr[c]);
+    for (int c0 = 32 * kKeptChunks; c0 < npart; c0 += 32) {
         const int i = c0 + lane;
         float wl = 0.f;
         if (i < npart) {
             const float mi = m[i];
             wl = (M == -CUDART_INF_F || mi == -CUDART_INF_F) ? 0.f : exp2f(mi - M);
         }
-        const int n = min(32, npart - c0);
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, wl, j);
-            const float* oj = o + (int64_t)(c0 + j) * D;
-            if constexpr (DPL == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(oj);
-                acc[0] = fmaf(wj, v.x, acc[0]);
-                acc[1] = fmaf(wj, v.y, acc[1]);
-                acc[2] = fmaf(wj, v.z, acc[2]);
-                acc[3] = fmaf(wj, v.w, acc[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2*>(oj);
-                acc[0] = fmaf(wj, v.x, acc[0]);
-                acc[1] = fmaf(wj, v.y, acc[1]);
-            }
-        }
+        accumulate(c0, min(32, npart - c0), wl);
     }
     store(acc, L > 0.f ? 1.f / L : 0.f);
 }

@@ -259,10 +259,12 @@ def test_repeated_decode_is_bit_identical(name):
 
 
 def test_lse_reduce_merges_oracle_partials():
-    """The reduce kernel alone, fed partials the oracle computed per range."""
+    """The reduce kernel alone, fed partials the oracle computed per range:
+    rows of 2 to 7 partials (one load round), 10 and 35 (partials' m and l
+    kept in registers) and 132 (past what the registers keep)."""
     rng = np.random.default_rng(11)
     BS, P, D, Hkv = 16, 32, 128, 2
-    ctx = [33, 64, 65, 200, 31]
+    ctx = [33, 64, 65, 200, 31, 300, 1100, 4200]
     kc, vc, q, bt, ctxa = _random_problem(rng, W.F16, W.F16, D, BS, 1, Hkv, ctx)
     S, Hq = len(ctx), Hkv
     maxp = -(-int(ctxa.max()) // P)
