@@ -19,8 +19,19 @@
  * Ownership.  The caller owns every buffer.  The library never allocates,
  *   frees or synchronises, and it is thread-safe.  Between calls it keeps only
  *   a per-device record of each decode kernel's launch size and a static
- *   device table of work counters (one slot per in-flight decode launch, 1024
- *   slots, each reset to zero by the launch that used it).
+ *   device table of work counters for the streaming decode kernel (the
+ *   single-head and FP8 decode): 1024 slots, each reset to zero by the last
+ *   CTA of the launch that used it.  A launch takes the next slot in turn
+ *   when it is issued, or captured into a CUDA graph (a graph keeps its slot
+ *   for every replay).  Two launches may therefore share a slot only if they
+ *   run at the same time: more than 1024 decode launches in flight at once,
+ *   or one captured decode graph replayed on two streams at once, or replayed
+ *   while the direct decode launch issued 1024 launches after its capture
+ *   (which takes the same slot) still runs on another stream.  Avoid those;
+ *   launches on one stream, and graph replays on one stream, never share a
+ *   slot.  A shared slot makes work items be skipped; the kernels then set
+ *   PKV_DEVERR_SCHED when they see it (more claims or finished CTAs than one
+ *   launch can make), though an overlap can go unseen.
  * Pointers.   "device" pointers must be CUDA device (or managed) memory of
  *   the current device.  Element data (caches, q, k, v, out) must be 16-byte
  *   aligned and dense row-major in the shapes given.
@@ -81,6 +92,9 @@ typedef enum pkv_dtype {
                                  /* ran out; that call's output is not valid   */
 #define PKV_DEVERR_PREFIX    32  /* a shared-prefix group entry is unusable, or */
                                  /* a member's table differs within the prefix */
+#define PKV_DEVERR_SCHED     64  /* a decode launch found its work-counter slot */
+                                 /* in use by another launch in flight; that   */
+                                 /* call's output is not valid (see Ownership) */
 
 /* One layer's cache.  k_cache / v_cache: device, caller-owned, layout above.
  * k_scale / v_scale: for an FP8 cache, the stored code times the scale is the
@@ -408,6 +422,9 @@ pkv_status pkv_paged_attention_prefill(const pkv_cache_desc* cache, const void* 
  *   different host threads) race on the array; issue them on one stream.
  * ------------------------------------------------------------------------- */
 #define PKV_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+/* (The address looked up on a device's first call belongs to that device's
+ * CUDA context: after cudaDeviceReset, do not call this entry point again in
+ * the same process.) */
 
 pkv_status pkv_paged_attention_decode_static_ws(const pkv_cache_desc* cache,
                                                 const void* q, int32_t q_dtype,
@@ -418,6 +435,22 @@ pkv_status pkv_paged_attention_decode_static_ws(const pkv_cache_desc* cache,
                                                 int32_t max_context_len, float scale,
                                                 int32_t partition_size, int32_t* dev_err,
                                                 void* out, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_testing_set_decode_wait_limit -- a testing aid, not part of the method
+ * (the pages have no counterpart).
+ *
+ * The streaming decode kernel waits on mbarriers for its own bulk copies, and
+ * every such wait is bounded: after the limit it sets PKV_DEVERR_TIMEOUT in
+ * dev_err, stops waiting everywhere, lets the copies it started land and
+ * returns, so the context stays usable.  This call sets the number of polls
+ * per wait for decode calls issued afterwards (captured into their launch
+ * parameters at the call): 0 restores the kernel's own limit (2^22 polls).  A
+ * test sets a small value to make a wait run out on purpose and check the
+ * error path.  Returns the previous setting.  Process-wide; the drain of
+ * copies in flight always keeps the full limit.
+ * ------------------------------------------------------------------------- */
+uint32_t pkv_testing_set_decode_wait_limit(uint32_t tries);
 
 #ifdef __cplusplus
 }

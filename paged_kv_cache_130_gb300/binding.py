@@ -26,6 +26,7 @@ PKV_STATIC_SCRATCH_BYTES = 32 << 20
 PKV_DEVERR_SLOT, PKV_DEVERR_BLOCK_ID, PKV_DEVERR_CONTEXT, PKV_DEVERR_COPY_PAIR = 1, 2, 4, 8
 PKV_DEVERR_TIMEOUT = 16
 PKV_DEVERR_PREFIX = 32
+PKV_DEVERR_SCHED = 64
 
 
 class PkvError(RuntimeError):
@@ -81,6 +82,7 @@ def load():
         "pkv_paged_attention_decode_shared_prefix": (i32, [dp, vp, i32, i32, i32, vp, i32, vp,
                                                            i32, i32, vp, vp, i32, i32, f32, i32,
                                                            vp, ctypes.c_size_t, vp, vp, vp]),
+        "pkv_testing_set_decode_wait_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -252,6 +254,13 @@ def pkv_paged_attention_decode_static_ws(cache, q, block_tables, context_lens, m
         int(partition_size), _ptr(dev_err), _ptr(out), _stream(stream)),
         "pkv_paged_attention_decode_static_ws")
     return out
+
+
+def pkv_testing_set_decode_wait_limit(tries):
+    """Polls per bounded wait of the streaming decode kernel for later decode
+    calls (0: the kernel's own limit); a testing aid.  Returns the previous
+    setting."""
+    return int(load().pkv_testing_set_decode_wait_limit(int(tries)))
 
 
 def pkv_shared_prefix_workspace_bytes(cache, num_seqs, num_heads, max_context_len,

@@ -101,14 +101,16 @@ __device__ __forceinline__ void consumers_sync(int nthreads)
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// Bounded wait for phase `parity` of `bar`.  Returns false when the CTA has
-// given up (time-out here or elsewhere); the caller then skips the stage.
+// Bounded wait for phase `parity` of `bar`: at most `tries` polls.  Returns
+// false when the CTA has given up (time-out here or elsewhere); the caller then
+// skips the stage.
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
-                                             volatile int* abort_flag, int32_t* dev_err)
+                                             volatile int* abort_flag, int32_t* dev_err,
+                                             uint32_t tries)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    for (uint32_t i = 0; i < tries; ++i) {
         if (mbar_try_wait(bar, parity))
             return true;
         if (*abort_flag)
@@ -304,7 +306,11 @@ struct StreamSmem {
     static constexpr int cur = items + 4 * kItemQueue;
     static constexpr int flags = cur + 8;
     static constexpr int abort = flags + 4 * S::NSTG;
-    static constexpr int ctx = abort + 16;
+    // the producer's records for the drain at the CTA's end: [0] one past the
+    // last ring tile armed, [1] publishes made, [2 + i] whether queue entry i's
+    // latest publish started a bulk copy of q
+    static constexpr int drain = abort + 16;
+    static constexpr int ctx = drain + 4 * (2 + kItemQueue);
     static constexpr int order = ctx + 4 * kCtxCache;
     static constexpr int QSLOT = ((D * 2 + 127) / 128) * 128;   // q row of one item
     static constexpr int qbuf = ((order + 4 * kSortMax + 127) / 128) * 128;
@@ -348,7 +354,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
     float* sm_m = reinterpret_cast<float*>(smem + L::merge_m);
     float* sm_l = reinterpret_cast<float*>(smem + L::merge_l);
     float* sm_acc = reinterpret_cast<float*>(smem + L::merge_acc);
+    volatile int* drain = reinterpret_cast<volatile int*>(smem + L::drain);
     unsigned char* qbuf = smem + L::qbuf;
+    // polls per wait on the ring and the item queue (a test may lower it to
+    // make a wait run out); the drain at the end always has the full limit
+    const uint32_t tries = p.wait_tries ? p.wait_tries : kSpinLimit;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -362,6 +372,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
             mbar_init(&iq_empty[i], 1);
         }
         *abort_flag = 0;
+        for (int i = 0; i < 2 + kItemQueue; ++i)
+            drain[i] = 0;
         mbar_init_fence();
     }
     // launched with programmatic dependent launch after whatever the stream
@@ -396,6 +408,111 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
     const int U = p.num_heads;
     const int64_t block_stride = (int64_t)p.num_kv_heads * TILE;
 
+    // -------------------------------------------------------------- consumers
+    // (a lambda, so that the producer and the consumers meet again at the end)
+    auto consumer_loop = [&]() {
+        const int ctid = threadIdx.x;                 // 0 .. NCT-1
+        const float qk = p.qk_scale_log2;
+        uint32_t t = 0;
+        for (int n = 0;; ++n) {
+            // warp 0 takes the next item from the queue and shares it (two slots,
+            // so a slow reader of item n never sees item n+1's value)
+            if (warp == 0) {
+                const int qs = n % kItemQueue;
+                const bool ok = __all_sync(
+                    0xffffffffu, wait_bounded(&iq_full[qs], (n / kItemQueue) & 1, abort_flag,
+                                              p.dev_err, tries));
+                const int item = ok ? items[qs] : -1;
+                __syncwarp();
+                if (lane == 0)
+                    cur[n & 1] = item;
+            }
+            consumers_sync(NCT);
+            const int item = cur[n & 1];
+            if (item < 0)
+                break;
+            const int u = item % U;
+            const int rest = item / U;
+            const int s = sorted ? sm_order[rest % p.num_seqs] : rest % p.num_seqs;
+            const int part = rest / p.num_seqs;
+            const int ctx = s < ncache ? sm_ctx[s] : __ldg(p.context_lens + s);
+            const PartitionWork w = dec::locate_ctx(p, s, part, ctx, ctid == 0);
+            const int head0 = u;
+            const int nrows = 1;
+            const int qs = n % kItemQueue;
+            const unsigned char* qrow_s = qbuf + qs * L::QSLOT;
+            if (w.zero_out || w.zero_partial) {
+                if (warp == 0 && lane == 0)
+                    mbar_arrive(&iq_empty[qs]);
+                dec::write_trivial<QT>(p, w, head0, nrows, ctid, NCT);
+                continue;
+            }
+            const int nblk = ceil_div_i(w.t_end - w.t_begin, BS);
+            const int k0 = (int)((warp + NC - (int)(t % NC)) % NC);
+            // every warp observes the entry's completion itself before reading
+            // the q rows the bulk copy wrote (the phase cannot move on before the
+            // entry is released below)
+            __all_sync(0xffffffffu, wait_bounded(&iq_full[qs], (n / kItemQueue) & 1, abort_flag,
+                                                 p.dev_err, tries));
+            {
+                using T = SimtTile<CT, D, BS>;
+                T st;
+                st.reset();
+                float qf[T::EPV];
+                {
+                    const unsigned char* qrow = qrow_s + (lane % T::RV) * T::EPV * 2;
+#pragma unroll
+                    for (int i = 0; i < T::EPV / 8; ++i)
+                        unpack_vec<QT>(ld_shared_v4(qrow + 16 * i), qf + 8 * i);
+#pragma unroll
+                    for (int e = 0; e < T::EPV; ++e)
+                        qf[e] *= qk;
+                }
+                const int tsub = lane / T::RV;
+                for (int k = k0; k < nblk; k += NC) {
+                    const uint32_t tt = t + k;
+                    const uint32_t stage = tt % NSTG;
+                    const bool ok = __all_sync(
+                        0xffffffffu, wait_bounded(&full[stage], (tt / NSTG) & 1, abort_flag,
+                                                  p.dev_err, tries));
+                    if (ok && flags[stage]) {
+                        const char* sk =
+                            reinterpret_cast<const char*>(ring + stage * Shape::STAGE);
+                        st.consume(sk, sk + Shape::VOFF, qf, lane, w.t_begin + k * BS + tsub,
+                                   w.t_end);
+                    }
+                    __syncwarp();
+                    if (ok && lane == 0)
+                        mbar_arrive(&empty[stage]);
+                }
+                st.finish_warp();
+                // filed by block residue k0, not by warp: the merge then adds the
+                // same partial sums in the same order whichever warp held a
+                // residue (that depends on the items the CTA took before), so a
+                // result is the same from run to run, bit for bit
+                if (lane < T::RV) {
+#pragma unroll
+                    for (int e = 0; e < T::EPV; ++e)
+                        sm_acc[k0 * D + lane * T::EPV + e] = st.acc(e);
+                }
+                if (lane == 0) {
+                    sm_m[k0] = st.m;
+                    sm_l[k0] = st.l;
+                }
+            }
+            t += nblk;
+            consumers_sync(NCT);
+            // every consumer warp has its q in registers: the queue entry is
+            // free -- unless a wait gave up (a warp whose wait on the entry
+            // failed raised the abort flag before this barrier): then the q
+            // copy may still be in flight, and the entry stays taken so that
+            // no new copy is started into it
+            if (warp == 0 && lane == 0 && !*abort_flag)
+                mbar_arrive(&iq_empty[qs]);
+            dec::finish_rows<QT, NC, 1>(p, w, head0, nrows, sm_m, sm_l, sm_acc, ctid, NCT);
+        }
+    };
+
     if (warp == NC) {
         // ---------------------------------------------------------- producer
         // Claims items, publishes each non-idle one to the consumers through
@@ -409,8 +526,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
             // of one (sequence, query head), streamed back to back so that
             // the claim's and the block table's round trips are paid once
             int unit = 0;
-            if (lane == 0)
+            if (lane == 0) {
                 unit = (int)atomicAdd(&g_sched[slot][0], 1u);
+                // one launch hands out at most num_items + gridDim.x claims:
+                // a higher count means another launch shares the slot
+                if ((unsigned)unit >= (unsigned)num_items + gridDim.x)
+                    flag_error(p.dev_err, PKV_DEVERR_SCHED);
+            }
             unit = __shfl_sync(0xffffffffu, unit, 0);
             const bool last = unit >= num_items;
             for (int sub = 0; sub < (last ? 1 : unit_parts); ++sub) {
@@ -436,10 +558,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
                 if (lane == 0) {
                     const bool ok = published < kItemQueue ||
                                     wait_bounded(&iq_empty[qs], ((published / kItemQueue) - 1) & 1,
-                                                 abort_flag, p.dev_err);
+                                                 abort_flag, p.dev_err, tries);
                     if (ok) {
                         items[qs] = last ? -1 : item;
-                        if (last || w.zero_out || w.zero_partial) {
+                        drain[1] = published + 1;
+                        const bool copy_q = !(last || w.zero_out || w.zero_partial);
+                        drain[2 + qs] = copy_q ? 1 : 0;
+                        if (!copy_q) {
                             mbar_arrive(&iq_full[qs]);
                         } else {
                             // the item's query rows travel with its queue entry
@@ -476,7 +601,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
                         int ok = 0;
                         if (lane == 0) {
                             ok = use == 0 || wait_bounded(&empty[stage], (use - 1) & 1, abort_flag,
-                                                          p.dev_err);
+                                                          p.dev_err, tries);
                             if (ok) {
                                 flags[stage] = valid ? 1 : 0;
                                 if (valid) {
@@ -486,6 +611,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
                                     mbar_arrive(&full[stage]);
                                 }
                                 armed = t + 1;
+                                drain[0] = (int)armed;
                             }
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -514,117 +640,41 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
             // this CTA takes no more items; the last CTA to get here resets the slot
             __threadfence();
             const unsigned int prev = atomicAdd(&g_sched[slot][1], 1u);
+            if (prev >= gridDim.x)
+                flag_error(p.dev_err, PKV_DEVERR_SCHED);   // another launch shares the slot
             if (prev == gridDim.x - 1) {
                 g_sched[slot][0] = 0u;
                 g_sched[slot][1] = 0u;
                 __threadfence();
             }
-            if (stop) {
-                // after a time-out, let the copies already started land (bounded)
-                const uint32_t first = armed > (uint32_t)NSTG ? armed - NSTG : 0;
-                for (uint32_t tt = first; tt < armed; ++tt)
-                    for (uint32_t i = 0; i < kSpinLimit; ++i)
-                        if (mbar_try_wait(&full[tt % NSTG], (tt / NSTG) & 1))
-                            break;
-            }
         }
-        return;
+    } else {
+        consumer_loop();
     }
-
-    // -------------------------------------------------------------- consumers
-    const int ctid = threadIdx.x;                 // 0 .. NCT-1
-    const float qk = p.qk_scale_log2;
-    uint32_t t = 0;
-    for (int n = 0;; ++n) {
-        // warp 0 takes the next item from the queue and shares it (two slots,
-        // so a slow reader of item n never sees item n+1's value)
-        if (warp == 0) {
-            const int qs = n % kItemQueue;
-            const bool ok = __all_sync(0xffffffffu, wait_bounded(&iq_full[qs], (n / kItemQueue) & 1,
-                                                                abort_flag, p.dev_err));
-            const int item = ok ? items[qs] : -1;
-            __syncwarp();
-            if (lane == 0)
-                cur[n & 1] = item;
+    // Every copy this CTA started lands before it exits.  In a run without a
+    // time-out the consumers waited for each one already; after one, the
+    // copies still in flight are the last NSTG ring tiles armed and the q rows
+    // of the last kItemQueue published items (the producer's records are
+    // final once every warp has reached this barrier).  These waits keep the
+    // full limit whatever the test setting.
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        const uint32_t armed_all = (uint32_t)drain[0];
+        const uint32_t first = armed_all > (uint32_t)NSTG ? armed_all - NSTG : 0;
+        for (uint32_t tt = first; tt < armed_all; ++tt)
+            for (uint32_t i = 0; i < kSpinLimit; ++i)
+                if (mbar_try_wait(&full[tt % NSTG], (tt / NSTG) & 1))
+                    break;
+        const int pub = drain[1];
+        for (int n = pub > kItemQueue ? pub - kItemQueue : 0; n < pub; ++n) {
+            if (!drain[2 + n % kItemQueue])
+                continue;
+            for (uint32_t i = 0; i < kSpinLimit; ++i)
+                if (mbar_try_wait(&iq_full[n % kItemQueue], (n / kItemQueue) & 1))
+                    break;
         }
-        consumers_sync(NCT);
-        const int item = cur[n & 1];
-        if (item < 0)
-            break;
-        const int u = item % U;
-        const int rest = item / U;
-        const int s = sorted ? sm_order[rest % p.num_seqs] : rest % p.num_seqs;
-        const int part = rest / p.num_seqs;
-        const int ctx = s < ncache ? sm_ctx[s] : __ldg(p.context_lens + s);
-        const PartitionWork w = dec::locate_ctx(p, s, part, ctx, ctid == 0);
-        const int head0 = u;
-        const int nrows = 1;
-        const int qs = n % kItemQueue;
-        const unsigned char* qrow_s = qbuf + qs * L::QSLOT;
-        if (w.zero_out || w.zero_partial) {
-            if (warp == 0 && lane == 0)
-                mbar_arrive(&iq_empty[qs]);
-            dec::write_trivial<QT>(p, w, head0, nrows, ctid, NCT);
-            continue;
-        }
-        const int nblk = ceil_div_i(w.t_end - w.t_begin, BS);
-        const int k0 = (int)((warp + NC - (int)(t % NC)) % NC);
-        // every warp observes the entry's completion itself before reading
-        // the q rows the bulk copy wrote (the phase cannot move on before the
-        // entry is released below)
-        __all_sync(0xffffffffu, wait_bounded(&iq_full[qs], (n / kItemQueue) & 1, abort_flag,
-                                             p.dev_err));
-        {
-            using T = SimtTile<CT, D, BS>;
-            T st;
-            st.reset();
-            float qf[T::EPV];
-            {
-                const unsigned char* qrow = qrow_s + (lane % T::RV) * T::EPV * 2;
-#pragma unroll
-                for (int i = 0; i < T::EPV / 8; ++i)
-                    unpack_vec<QT>(ld_shared_v4(qrow + 16 * i), qf + 8 * i);
-#pragma unroll
-                for (int e = 0; e < T::EPV; ++e)
-                    qf[e] *= qk;
-            }
-            const int tsub = lane / T::RV;
-            for (int k = k0; k < nblk; k += NC) {
-                const uint32_t tt = t + k;
-                const uint32_t stage = tt % NSTG;
-                const bool ok = __all_sync(0xffffffffu, wait_bounded(&full[stage], (tt / NSTG) & 1,
-                                                                    abort_flag, p.dev_err));
-                if (ok && flags[stage]) {
-                    const char* sk = reinterpret_cast<const char*>(ring + stage * Shape::STAGE);
-                    st.consume(sk, sk + Shape::VOFF, qf, lane, w.t_begin + k * BS + tsub, w.t_end);
-                }
-                __syncwarp();
-                if (ok && lane == 0)
-                    mbar_arrive(&empty[stage]);
-            }
-            st.finish_warp();
-            // filed by block residue k0, not by warp: the merge then adds the
-            // same partial sums in the same order whichever warp held a
-            // residue (that depends on the items the CTA took before), so a
-            // result is the same from run to run, bit for bit
-            if (lane < T::RV) {
-#pragma unroll
-                for (int e = 0; e < T::EPV; ++e)
-                    sm_acc[k0 * D + lane * T::EPV + e] = st.acc(e);
-            }
-            if (lane == 0) {
-                sm_m[k0] = st.m;
-                sm_l[k0] = st.l;
-            }
-        }
-        t += nblk;
-        consumers_sync(NCT);
-        // every consumer warp has its q in registers: the queue entry is free
-        if (warp == 0 && lane == 0)
-            mbar_arrive(&iq_empty[qs]);
-        dec::finish_rows<QT, NC, 1>(p, w, head0, nrows, sm_m, sm_l, sm_acc, ctid, NCT);
     }
-    if (p.wait_prior && ctid == 0)
+    if (p.wait_prior && threadIdx.x == 0)
         pdl_wait_primary();
 }
 

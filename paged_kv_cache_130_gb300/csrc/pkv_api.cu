@@ -219,6 +219,7 @@ pkv::DecodeParams decode_params(const pkv_cache_desc* cache, const void* q, int3
     p.max_group_size = grp.max_size;
     p.max_prefix_blocks = grp.max_blocks;
     p.prefix_partition = grp.partition;
+    p.wait_tries = pkv::decode_wait_tries();
     return p;
 }
 
@@ -299,9 +300,24 @@ pkv_status check_workspace(const WorkspaceLayout& wl, const void* workspace, siz
     return PKV_OK;
 }
 
+// The wait limit that pkv_testing_set_decode_wait_limit sets (0 = the
+// kernels' own).
+std::atomic<uint32_t> g_decode_wait_tries{0};
+
 }  // namespace
 
+uint32_t pkv::decode_wait_tries()
+{
+    return g_decode_wait_tries.load(std::memory_order_relaxed);
+}
+
 extern "C" {
+
+uint32_t pkv_testing_set_decode_wait_limit(uint32_t tries)
+{
+    return g_decode_wait_tries.exchange(tries, std::memory_order_relaxed);
+}
+
 
 const char* pkv_status_string(int32_t status)
 {

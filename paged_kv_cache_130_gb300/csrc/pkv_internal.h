@@ -50,7 +50,15 @@ struct DecodeParams {
     // for it (griddepcontrol.wait) only before its CTAs exit, so that its own
     // completion implies the prefix kernel's.
     int32_t wait_prior;
+    // Polls per bounded mbarrier wait of the streaming kernel's ring and item
+    // queue; 0 = the kernel's own limit.  Only tests set it (to make a wait
+    // run out on purpose); the drain of copies in flight ignores it.
+    uint32_t wait_tries;
 };
+
+// Process-wide wait-limit setting that the decode entry points copy into
+// DecodeParams::wait_tries (pkv_testing_set_decode_wait_limit).
+uint32_t decode_wait_tries();
 
 struct ReduceParams {
     int32_t num_seqs;

@@ -9,3 +9,15 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (parity tests through the C ABI)")
     config.addinivalue_line("markers", "slow: full-size workload")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the worst err / bound ratio of each attention parity check, so
+    the margin under the tolerance is visible in the run's output."""
+    h = sys.modules.get("harness")
+    worst = getattr(h, "WORST_RATIO", None) if h is not None else None
+    if not worst:
+        return
+    terminalreporter.write_sep("-", "attention parity: worst |err| / bound per check")
+    for name in sorted(worst):
+        terminalreporter.write_line("%-60s %.3f" % (name, worst[name]))

@@ -200,21 +200,35 @@ def half_ulp(ref, out_dtype):
 
 
 def assert_attention_close(got, ref, what="", out_dtype=W.F16):
-    """|got - ref| <= 2e-3 + 2e-3 |ref| elementwise for the kernel's fp32
-    result; the output is that result rounded once to fp16 / bf16, so the
-    check allows that rounding (half an ulp of the output type) on top."""
+    """|got - ref| <= 2e-3 + 2e-3 |ref| elementwise.
+
+    For bf16 outputs the bound also allows half an ulp of bf16 at |ref|: the
+    kernel's fp32 result is rounded once to bf16, and that rounding alone can
+    move a value by up to 2^-8 |ref|, more than 2e-3 |ref|.  For fp16 outputs
+    half an ulp is at most 2^-11 |ref|, which the plain bound already covers,
+    so fp16 outputs are held to the plain bound.  Returns the worst
+    err / bound ratio (also recorded in WORST_RATIO under `what`)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), "%s: non-finite output" % what
     err = np.abs(got - ref)
-    bound = ATOL + RTOL * np.abs(ref) + half_ulp(ref, out_dtype)
+    bound = ATOL + RTOL * np.abs(ref)
+    if out_dtype == W.BF16:
+        bound = bound + half_ulp(ref, out_dtype)
     bad = err > bound
     if bad.any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError("%s: %d of %d outside tolerance; worst at %s: got %r ref %r"
                              % (what, int(bad.sum()), bad.size, i, got[i], ref[i]))
-    return float(err.max()) if err.size else 0.0
+    ratio = float((err / bound).max()) if err.size else 0.0
+    key = "%s (%s)" % (what, "bf16" if out_dtype == W.BF16 else "fp16")
+    WORST_RATIO[key] = max(ratio, WORST_RATIO.get(key, 0.0))
+    return ratio
+
+
+# worst err / bound ratio seen per check name during the session
+WORST_RATIO = {}
 
 
 def gpu_available():
@@ -227,11 +241,7 @@ def oracle_threads():
 
 def segment_sequences(w, seg):
     """Sequences whose tokens a prefill segment holds."""
-    if w.name == "cow_parallel_sampling_f16":
-        samples = w.num_seqs // int(w.notes["tails"].shape[0])
-        p = seg.key[1]
-        return set(range(p * samples, (p + 1) * samples))
-    return {seg.key[1]}
+    return w.segment_sequences(seg)
 
 
 def prefill_both(w, g, o, only=None, threads=8):
