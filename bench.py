@@ -9,10 +9,13 @@ inputs of every benchmark layer exceed the 129 MB L2, so no flush is needed
 (``--flush write`` adds a 512 MiB write between steps).
 
 Output: one JSON line on rank 0.  ``value`` is decode KV-read GB/s: algorithmic
-bytes of one decode (every cached K/V element once per KV head, q, out, the used
-block-table entries and the context lengths) over the decode time measured with
-CUDA events on the launch stream, summed over all ranks' work and divided by the
-slowest rank's time (replicas: every rank decodes its own batch).
+bytes of one decode (every cached K/V element once per KV head -- a block that
+forked sequences share is counted once when the shared-prefix call reads it
+once --, q, out, the used block-table entries and the context lengths) over the
+decode time measured with CUDA events on the launch stream, summed over all
+ranks' work and divided by the slowest rank's time (replicas: every rank
+decodes its own batch).  The default run (OPT-13B layer) also times the GQA,
+copy-on-write and long E4M3 layers the same way, under ``configs``.
 
 ``--impl reference`` times the CPU oracle on the host cores on a bounded sample
 of the same workload instead (rank 0 only).
@@ -128,6 +131,11 @@ def parse_args(argv=None):
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="a smaller batch of the same decode workload (profiler "
                          "captures); the line's config names the batch")
+    ap.add_argument("--configs", default="auto",
+                    help="auto: the default run also times the other decode workloads "
+                         "(GQA, copy-on-write parallel sampling, long E4M3) under a "
+                         "`configs` key; none: the headline workload only; or a "
+                         "comma-separated list of workload names")
     ap.add_argument("--flush", default="none", choices=["none", "write"],
                     help="none: the decode inputs alone exceed L2; write: also write "
                          "512 MiB between steps")
@@ -269,14 +277,21 @@ def sample_bytes(w, seqs):
 
 
 class HostState:
-    """Host caches written through the oracle (the CPU arm's inputs)."""
+    """Host caches written through the oracle (the CPU arm's inputs).
 
-    def __init__(self, w, prefill):
+    `prefill`: the workload's (slots, k, v) batches, or None to draw the
+    segments here; `seqs`: only the segments these sequences read (all when
+    None).  The copy-on-write pairs and the step's tokens are always applied."""
+
+    def __init__(self, w, prefill=None, seqs=None, threads=8):
         import oracle
         shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
         dt = np.uint8 if w.cache_elem_bytes == 1 else np.uint16
         self.k_cache = np.zeros(shape, dt)
         self.v_cache = np.zeros(shape, dt)
+        if prefill is None:
+            segs = w.segments if seqs is None else w.segments_of(seqs)
+            prefill = w.prefill(threads=threads, segments=segs)
         for slots, k, v in prefill:
             oracle.kv_append(self.k_cache, self.v_cache, w.cache_dtype, k, v, w.io_dtype, slots,
                              w.k_scale, w.v_scale)
@@ -287,12 +302,22 @@ class HostState:
                          w.step_slots, w.k_scale, w.v_scale)
 
 
-def pick_sample(w, budget_s, host_state):
-    """Sequences and repetitions for a bounded oracle run (~budget_s seconds)."""
-    seqs = np.arange(w.num_seqs)
+def sample_sequences(w, cap_bytes):
+    """Leading sequences whose K/V fit `cap_bytes` (at least one): the part
+    of a workload the host prepares for a bounded oracle run."""
+    per = (w.context_lens.astype(np.int64) * w.num_kv_heads * w.head_dim * 2
+           * w.cache_elem_bytes)
+    n = int(np.searchsorted(np.cumsum(per), cap_bytes, side="right"))
+    return np.arange(max(1, min(w.num_seqs, n)))
+
+
+def pick_sample(w, budget_s, host_state, seqs=None):
+    """Sequences (out of `seqs`, default all) and repetitions for a bounded
+    oracle run (~budget_s seconds)."""
+    seqs = np.arange(w.num_seqs) if seqs is None else np.asarray(seqs)
     one = oracle_decode_sample(w, host_state, seqs[:1], 1)
     per_seq = max(one, 1e-4)
-    n = int(min(w.num_seqs, max(1, budget_s / per_seq)))
+    n = int(min(len(seqs), max(1, budget_s / per_seq)))
     seqs = seqs[:n]
     reps = 1
     t = oracle_decode_sample(w, host_state, seqs, 1)
@@ -301,7 +326,7 @@ def pick_sample(w, budget_s, host_state):
     return seqs, reps
 
 
-def run_reference(args, w, prefill):
+def run_reference(args, w, prefill=None):
     world, rank, _ = dist_env()
     if rank != 0:
         return None
@@ -343,15 +368,17 @@ def workload_config(w):
             "parallelism": "replicas"}
 
 
-def run_gpu(args, w, prefill):
+def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
+    """Time the decode step of workload `w` on this rank's GPU; returns the
+    JSON line (rank 0) or None.  The cache is filled from the workload's
+    seeded values, drawn in a thread pool; the oracle's CPU baseline runs on
+    the sequences whose K/V fit `sample_cap_bytes` (all when None)."""
     import torch
     import torch.distributed as dist
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group("nccl", device_id=dev)
 
     from paged_kv_cache_130_gb300 import binding as B
     from paged_kv_cache_130_gb300 import build as pkv_build
@@ -371,7 +398,7 @@ def run_gpu(args, w, prefill):
     def dev16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(iodt).to(dev)
 
-    for slots, k, v in prefill:
+    for slots, k, v in w.prefill(threads=threads):
         B.pkv_kv_append(desc, dev16(k), dev16(v), torch.from_numpy(slots).to(dev))
     q = dev16(w.q)
     bt = torch.from_numpy(w.block_tables).to(dev)
@@ -512,7 +539,11 @@ def run_gpu(args, w, prefill):
     step_s = sum(step_ms) / 1e3
     dbytes = w.decode_bytes()
     dec_s, step_s = slowest([dec_s, step_s], dev)
-    value = whole_job_rate(dbytes * args.steps, dec_s, world) / 1e9
+    # bytes the decode call must read: with shared prefixes every distinct
+    # block once (the prefix is read once per group), else every sequence's
+    # K/V; `value` counts these, never a shared block once per member
+    rbytes = dbytes - w.kv_bytes() + w.unique_kv_bytes() if shared else dbytes
+    value = whole_job_rate(rbytes * args.steps, dec_s, world) / 1e9
 
     # end to end through the C ABI from pinned host buffers: the step's
     # inputs are packed into one pinned staging buffer and cross with one
@@ -560,44 +591,55 @@ def run_gpu(args, w, prefill):
             step_e2e()
             h_out.copy_(out, non_blocking=True)
 
-        run_e2e = e2e_once
+        def time_e2e(run):
+            ms = []
+            for i in range(args.steps + args.warmup):
+                maybe_flush(i)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                run()
+                b.record()
+                b.synchronize()
+                if i >= args.warmup:
+                    ms.append(a.elapsed_time(b))
+            sec = slowest([sum(ms) / 1e3], dev)[0]
+            return {"value": whole_job_rate(rbytes * args.steps, sec, world) / 1e9,
+                    "ms_per_step": sec * 1e3 / args.steps}
+
+        # every step runs the C-ABI host code (argument checks, partition
+        # choice, launches) between the events, as a caller's step does
+        direct = time_e2e(e2e_once)
+        e2e = {"value": direct["value"], "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": direct["ms_per_step"],
+               "timing": "per step, between CUDA events: the pinned host-to-device copy of "
+                         "the packed inputs, the C-ABI calls made from Python (host checks "
+                         "and kernel launches included), the device-to-host copy of out"}
         if not args.no_graphs:
-            # the copies and the C-ABI calls of one step as one CUDA graph, so
-            # the host's call overhead stays out of the device timeline
+            # the same copies and C-ABI launches captured once into a CUDA
+            # graph: a replay runs the kernels and copies only (the calls'
+            # host code ran at capture)
             e2e_once()
             torch.cuda.synchronize()
             ge = torch.cuda.CUDAGraph()
             with torch.cuda.graph(ge, stream=stream):
                 e2e_once()
             torch.cuda.synchronize()
-            run_e2e = ge.replay
-        e2e_ms = []
-        for i in range(args.steps + args.warmup):
-            maybe_flush(i)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            run_e2e()
-            b.record()
-            b.synchronize()
-            if i >= args.warmup:
-                e2e_ms.append(a.elapsed_time(b))
-        e2e_s = sum(e2e_ms) / 1e3
-        e2e_s = slowest([e2e_s], dev)[0]
-        e2e = {"value": whole_job_rate(dbytes * args.steps, e2e_s, world) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_s * 1e3 / args.steps}
+            gr = time_e2e(ge.replay)
+            e2e["graph_replay"] = {
+                "value": gr["value"], "unit": "GB/s", "ms_per_step": gr["ms_per_step"],
+                "timing": "graph replay of the captured C-ABI launches (copies and kernels "
+                          "only; no host code of the calls in the timed region)"}
 
     peak, peak_kind = hbm_peak()
     part_mean = sum(part_ms) / len(part_ms) / 1e3
-    # bytes the timed kernel must move: with shared prefixes every distinct
-    # block once (the prefix kernel reads a shared block once per group)
-    rbytes = dbytes - w.kv_bytes() + w.unique_kv_bytes() if shared else dbytes
     achieved = rbytes / part_mean / 1e9
     tr = NCU_TRAFFIC.get(w.name + (":shared-prefix" if shared else ""))
     traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == decode_src_sha() else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
+                "traffic_source": tr.get("profile") if tr and traffic is not None else None,
                 "kernel": ("shared-prefix decode call: decode_mma_kernel over the prefixes, "
                            + decode_kernel_name(w) + " over the rest, lse_reduce_kernel"
                            if shared else
@@ -610,10 +652,10 @@ def run_gpu(args, w, prefill):
     cfg["l2"] = ("decode inputs (%.0f MB of K/V per step) exceed the 129 MB L2; no flush"
                  % (w.kv_bytes() / 1e6) if args.flush == "none"
                  else "512 MiB written between steps (L2 flush)")
-    cfg["timing"] = ("CUDA events around CUDA-graph replays; e2e: one graph per step of one "
-                     "pinned host-to-device staging copy, the C-ABI calls and the output's "
-                     "device-to-host copy") if not args.no_graphs \
-        else "CUDA events around direct calls"
+    cfg["timing"] = ("value: CUDA events around CUDA-graph replays of the decode call; "
+                     "roofline: the partition kernel launched `steps` times back to back "
+                     "between one pair of events; e2e: see e2e.timing") \
+        if not args.no_graphs else "CUDA events around direct calls"
     cfg["partition_size"] = ps
     cfg["shared_prefix"] = ({"groups": int(len(grp_blocks)), "max_group": max_group,
                              "prefix_blocks": max_prefix} if shared else None)
@@ -635,14 +677,16 @@ def run_gpu(args, w, prefill):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk, "wall_s": t_wall}
     if w.unique_kv_bytes() != w.kv_bytes():
-        # shared prompt blocks: the same figure over distinct bytes only
-        ubytes = dbytes - w.kv_bytes() + w.unique_kv_bytes()
-        line["unique_bytes_gbs"] = ubytes * args.steps * world / dec_s / 1e9
+        # shared prompt blocks: every sequence's K/V counted in full (a shared
+        # block once per member), the decode's logical work
+        line["logical_bytes_gbs"] = dbytes * args.steps * world / dec_s / 1e9
+    del replay, stages
     if world > 1:
         dist.barrier()
     if rank == 0 and not args.no_cpu_baseline:
-        hs = HostState(w, prefill)
-        seqs, reps = pick_sample(w, 15.0, hs)
+        cand = None if sample_cap_bytes is None else sample_sequences(w, sample_cap_bytes)
+        hs = HostState(w, seqs=cand, threads=threads)
+        seqs, reps = pick_sample(w, cpu_budget_s, hs, cand)
         t = oracle_decode_sample(w, hs, seqs, reps)
         line["cpu_baseline"] = {
             "value": sample_bytes(w, seqs) * reps / t / 1e9, "unit": "GB/s",
@@ -650,9 +694,23 @@ def run_gpu(args, w, prefill):
             "sample": "oracle decode of %d of %d sequences x %d repetitions (%d context tokens "
                       "each), fp64, all host threads" % (len(seqs), w.num_seqs, reps,
                                                         int(w.context_lens[seqs].sum()))}
-    if world > 1 and dist.is_initialized():
-        dist.destroy_process_group()
     return line if rank == 0 else None
+
+
+# the other decode workloads of the default run, each timed like the headline
+EXTRA_CONFIGS = ("llama2_70b_bf16_gqa", "cow_parallel_sampling_f16", "llama2_7b_fp8_long")
+# host K/V a config's bounded oracle sample is drawn from (the E4M3 layer
+# holds 2.5 GB; drawing all of it again for the CPU baseline would take minutes)
+EXTRA_SAMPLE_CAP = 400 << 20
+
+
+def config_summary(line):
+    """The per-config entry of the default run's `configs` key."""
+    keep = ("value", "unit", "hbm_frac", "decode_ms", "ms_per_step", "decode_tokens_per_s",
+            "model_tokens_per_s_attention_only", "decode_ms_spread", "decode_bytes",
+            "unique_kv_bytes", "logical_bytes_gbs", "roofline", "e2e", "gpu_launches", "clocks",
+            "cpu_baseline", "config")
+    return {k: line[k] for k in keep if k in line}
 
 
 # ------------------------------------------------------------------ prefill arm
@@ -1222,7 +1280,7 @@ def run_gpu_hash(args, w):
 def main(argv=None):
     args = parse_args(argv)
     from paged_kv_cache_130_gb300 import workloads as W
-    world, rank, _ = dist_env()
+    world, rank, local = dist_env()
     if args.impl == "reference" and rank != 0:
         return 0
     w = W.make(args.workload) if args.num_seqs is None else \
@@ -1237,12 +1295,44 @@ def main(argv=None):
         if line is not None:
             print(json.dumps(line), flush=True)
         return 0
-    prefill = list(w.prefill())
     if w.cu_seqlens_q is not None:
+        prefill = list(w.prefill())
         run = run_reference_prefill if args.impl == "reference" else run_gpu_prefill
-    else:
-        run = run_reference if args.impl == "reference" else run_gpu
-    line = run(args, w, prefill)
+        line = run(args, w, prefill)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    if args.impl == "reference":
+        line = run_reference(args, w)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_gpu(args, w)
+    extra = ()
+    if args.configs == "auto":
+        extra = EXTRA_CONFIGS if args.workload == DEFAULT_WORKLOAD and args.num_seqs is None \
+            else ()
+    elif args.configs != "none":
+        extra = tuple(n for n in args.configs.split(",") if n and n != args.workload)
+    if extra:
+        configs = {w.name: config_summary(line) if line is not None else None}
+        for name in extra:
+            torch.cuda.empty_cache()
+            w2 = W.make(name)
+            line2 = run_gpu(args, w2, cpu_budget_s=4.0, sample_cap_bytes=EXTRA_SAMPLE_CAP)
+            if line2 is not None:
+                configs[name] = config_summary(line2)
+            del w2
+        if line is not None:
+            line["configs"] = configs
+    if world > 1 and dist.is_initialized():
+        dist.destroy_process_group()
     if line is not None:
         print(json.dumps(line), flush=True)
     return 0

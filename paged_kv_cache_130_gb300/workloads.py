@@ -124,11 +124,43 @@ class Workload:
     def step_values(self):
         return self.values(self.step_key, len(self.step_slots))
 
-    def prefill(self):
-        """Iterate (slots, k_bits, v_bits) over the prefill segments."""
-        for seg in self.segments:
-            k, v = self.values(seg.key, len(seg.slots))
-            yield seg.slots, k, v
+    def prefill(self, threads=1, segments=None):
+        """Iterate (slots, k_bits, v_bits) over the prefill segments (or the
+        given ones), in order.  With threads > 1 the values of the next
+        segments are drawn ahead in a thread pool (each segment has its own
+        generator, so the values are the same either way)."""
+        segs = self.segments if segments is None else segments
+        if threads <= 1:
+            for seg in segs:
+                k, v = self.values(seg.key, len(seg.slots))
+                yield seg.slots, k, v
+            return
+        import concurrent.futures as cf
+        ahead = 2 * threads
+        with cf.ThreadPoolExecutor(threads) as ex:
+            futs = [ex.submit(self.values, sg.key, len(sg.slots)) for sg in segs[:ahead]]
+            for i, seg in enumerate(segs):
+                k, v = futs[i].result()
+                futs[i] = None
+                if i + ahead < len(segs):
+                    nxt = segs[i + ahead]
+                    futs.append(ex.submit(self.values, nxt.key, len(nxt.slots)))
+                yield seg.slots, k, v
+
+    def segment_sequences(self, seg):
+        """Sequences whose context holds a prefill segment's tokens: one
+        sequence, or every sample of a shared prompt."""
+        tails = self.notes.get("tails")
+        if tails is not None:
+            samples = int(tails.shape[1])
+            p = seg.key[1]
+            return set(range(p * samples, (p + 1) * samples))
+        return {seg.key[1]}
+
+    def segments_of(self, seqs):
+        """The prefill segments that the given sequences read."""
+        want = set(int(s) for s in seqs)
+        return [seg for seg in self.segments if self.segment_sequences(seg) & want]
 
     # ------------------------------------------------------------ sizes
     @property
@@ -211,17 +243,28 @@ class Workload:
         return int(self.copy_pairs.shape[0]) * 2 * 2 * blk
 
     # ------------------------------------------------------------ scales
-    def calibrate_fp8_scales(self):
-        """One scale per tensor: amax of every value written / 448 (fp32)."""
+    def calibrate_fp8_scales(self, threads=None):
+        """One scale per tensor: amax of every value written / 448 (fp32).
+        The segments are drawn in a thread pool (a maximum does not depend on
+        the order)."""
         if self.cache_dtype != E4M3:
             return
-        amax_k = np.float32(0.0)
-        amax_v = np.float32(0.0)
-        batches = list(self.prefill())
-        batches.append((self.step_slots,) + tuple(self.step_values()))
-        for _, k, v in batches:
-            amax_k = max(amax_k, np.abs(bits_to_float32(k, self.io_dtype)).max(initial=0))
-            amax_v = max(amax_v, np.abs(bits_to_float32(v, self.io_dtype)).max(initial=0))
+        import concurrent.futures as cf
+        import os
+
+        def amax(key, n):
+            k, v = self.values(key, n)
+            return (np.abs(bits_to_float32(k, self.io_dtype)).max(initial=0),
+                    np.abs(bits_to_float32(v, self.io_dtype)).max(initial=0))
+
+        jobs = [(seg.key, len(seg.slots)) for seg in self.segments]
+        jobs.append((self.step_key, len(self.step_slots)))
+        if threads is None:
+            threads = min(16, os.cpu_count() or 1)
+        with cf.ThreadPoolExecutor(max(1, threads)) as ex:
+            found = list(ex.map(lambda j: amax(*j), jobs))
+        amax_k = np.float32(max((a for a, _ in found), default=0.0))
+        amax_v = np.float32(max((b for _, b in found), default=0.0))
         self.k_scale = float(np.float32(amax_k) / np.float32(E4M3_MAX)) if amax_k > 0 else 1.0
         self.v_scale = float(np.float32(amax_v) / np.float32(E4M3_MAX)) if amax_v > 0 else 1.0
 
