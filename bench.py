@@ -104,6 +104,18 @@ def shares_prefixes(w):
             and w.block_size in (16, 32) and w.head_dim in (64, 128))
 
 
+def shared_single_pass(w, max_group, sms):
+    """Whether the library decodes this batch's shared prefixes in a single
+    pass: partition size left to the library, contexts of at most 4096
+    tokens, and at least one (group, KV head, row tile) CTA per SM."""
+    group = w.num_heads // w.num_kv_heads
+    rows = max_group * group
+    rt = 16 if rows > 8 else 8
+    _, blocks = w.prefix_groups()
+    ctas = len(blocks) * (-(-rows // rt)) * w.num_kv_heads
+    return w.partition_size == 0 and w.max_context_len <= 4096 and ctas >= sms
+
+
 def decode_kernel_name(w):
     """Which partition kernel the library runs for this workload: grouped
     16-bit heads go to the tensor-core kernel, everything else streams."""
@@ -412,6 +424,7 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
     grp_begin, grp_blocks = w.prefix_groups()
     shared = (args.shared_prefix == "auto" and int(grp_blocks.max(initial=0)) > 0
               and shares_prefixes(w))
+    single = False
     if shared:
         gb = torch.from_numpy(grp_begin).to(dev)
         gp = torch.from_numpy(grp_blocks).to(dev)
@@ -419,6 +432,13 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
         max_prefix = int(grp_blocks.max())
         ws_bytes = B.pkv_shared_prefix_workspace_bytes(desc, w.num_seqs, w.num_heads,
                                                        w.max_context_len, ps)
+        # the library's route for this call (the workload leaves the split to
+        # the library, partition size 0): the single pass when its CTAs cover
+        # the GPU, as pkv_testing_set_shared_prefix_path documents
+        single = shared_single_pass(w, max_group, torch.cuda.get_device_properties(dev)
+                                    .multi_processor_count)
+        # the split route's partition size, as the library resolves it
+        shared_ps = w.partition_size
     else:
         ws_bytes = B.pkv_decode_workspace_bytes(desc, w.num_seqs, w.num_heads,
                                                 w.max_context_len, ps)
@@ -429,7 +449,7 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
     maxp = -(-w.max_context_len // ps)
     launches_per_step = 1 + (1 if pairs is not None else 0) + 1 + (1 if maxp > 1 else 0)
     if shared:
-        launches_per_step = 1 + (1 if pairs is not None else 0) + 3
+        launches_per_step = 1 + (1 if pairs is not None else 0) + (1 if single else 3)
 
     def pre():
         if pairs is not None:
@@ -440,7 +460,7 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
         if shared:
             B.pkv_paged_attention_decode_shared_prefix(
                 desc, q, bt, cl, w.max_context_len, gb, gp, max_group, max_prefix, w.scale,
-                partition_size=ps, workspace=workspace, out=out)
+                partition_size=shared_ps, workspace=workspace, out=out)
         else:
             B.pkv_paged_attention_decode(desc, q, bt, cl, w.max_context_len, w.scale,
                                          partition_size=ps, workspace=workspace, out=out)
@@ -579,7 +599,7 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
             if shared:
                 B.pkv_paged_attention_decode_shared_prefix(
                     desc, views["q"], views["bt"], views["cl"], w.max_context_len, views["gb"],
-                    views["gp"], max_group, max_prefix, w.scale, partition_size=ps,
+                    views["gp"], max_group, max_prefix, w.scale, partition_size=shared_ps,
                     workspace=workspace, out=out)
             else:
                 B.pkv_paged_attention_decode(desc, views["q"], views["bt"], views["cl"],
@@ -640,7 +660,9 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "traffic_source": tr.get("profile") if tr and traffic is not None else None,
-                "kernel": ("shared-prefix decode call: decode_mma_kernel over the prefixes, "
+                "kernel": ("shared-prefix decode call, single pass: decode_group_kernel"
+                           if single else
+                           "shared-prefix decode call: decode_mma_kernel over the prefixes, "
                            + decode_kernel_name(w) + " over the rest, lse_reduce_kernel"
                            if shared else
                            decode_kernel_name(w) + " (pkv_paged_attention_partitions)"),
@@ -658,7 +680,9 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
         if not args.no_graphs else "CUDA events around direct calls"
     cfg["partition_size"] = ps
     cfg["shared_prefix"] = ({"groups": int(len(grp_blocks)), "max_group": max_group,
-                             "prefix_blocks": max_prefix} if shared else None)
+                             "prefix_blocks": max_prefix,
+                             "route": "single pass" if single else "split"}
+                            if shared else None)
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3 / args.steps, "higher_is_better": True,

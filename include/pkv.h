@@ -338,14 +338,21 @@ pkv_status pkv_lse_reduce(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
  *                      the partitions of the rest of the context).
  * Device checks (with dev_err): a group entry out of range or a prefix above
  * max_prefix_blocks flags PKV_DEVERR_PREFIX and that group's prefix is not
- * computed; a member past max_group_size or with a context shorter than its
- * prefix flags PKV_DEVERR_CONTEXT and its output is zero; a member whose table
- * differs from the first member's inside the prefix flags PKV_DEVERR_PREFIX
- * (its output then uses the first member's blocks).
+ * computed (its members' outputs are then zero, flagged PKV_DEVERR_CONTEXT,
+ * as far as the group's bounds can be used); a member past max_group_size or
+ * with a context shorter than its prefix flags PKV_DEVERR_CONTEXT and its
+ * output is zero; a member whose table differs from the first member's inside
+ * the prefix flags PKV_DEVERR_PREFIX (its output then uses the first member's
+ * blocks).
  * Supported: F16 or BF16 caches with q of the same type, 1..16 query heads per
  * KV head; anything else returns PKV_ERR_UNSUPPORTED and launches nothing.
  * num_groups == 0 or max_prefix_blocks == 0 gives the plain decode.
- * Launches: prefix kernel, partition kernel, reduce.
+ * Launches: with partition_size 0, max_context_len <= 4096 and at least one
+ *   (group, KV head, row tile) per SM, one kernel: each CTA reads its group's
+ *   shared blocks once for its rows, then each member's own blocks for that
+ *   member's rows, keeps one online softmax per row and writes out (the
+ *   workspace is not touched).  Otherwise three: prefix kernel, partition
+ *   kernel, reduce.  Both compute the attention defined above.
  * ------------------------------------------------------------------------- */
 size_t pkv_shared_prefix_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
                                          int32_t num_heads, int32_t max_context_len,
@@ -451,6 +458,23 @@ pkv_status pkv_paged_attention_decode_static_ws(const pkv_cache_desc* cache,
  * copies in flight always keeps the full limit.
  * ------------------------------------------------------------------------- */
 uint32_t pkv_testing_set_decode_wait_limit(uint32_t tries);
+
+/* ---------------------------------------------------------------------------
+ * pkv_testing_set_shared_prefix_path -- a testing aid, not part of the method
+ * (the pages have no counterpart).
+ *
+ * pkv_paged_attention_decode_shared_prefix computes the same attention by one
+ * of two routes: a single pass (one kernel; each CTA reads a group's shared
+ * blocks once for its rows, then each member's own blocks, and writes out
+ * directly), or a split (prefix kernel + partition kernel + log-sum-exp
+ * reduce over the workspace).  The library takes the single pass when
+ * partition_size is 0, max_context_len <= 4096 and the single pass has at
+ * least one CTA per SM; the split otherwise.  This call overrides that choice
+ * for later calls: 0 = the library's choice, 1 = always the single pass (the
+ * partition size is then unused), 2 = always the split.  Returns the previous
+ * setting, or -1 (and changes nothing) for another value.  Process-wide.
+ * ------------------------------------------------------------------------- */
+int32_t pkv_testing_set_shared_prefix_path(int32_t path);
 
 #ifdef __cplusplus
 }

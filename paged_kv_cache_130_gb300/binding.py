@@ -83,6 +83,7 @@ def load():
                                                            i32, i32, vp, vp, i32, i32, f32, i32,
                                                            vp, ctypes.c_size_t, vp, vp, vp]),
         "pkv_testing_set_decode_wait_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
+        "pkv_testing_set_shared_prefix_path": (i32, [i32]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -261,6 +262,16 @@ def pkv_testing_set_decode_wait_limit(tries):
     calls (0: the kernel's own limit); a testing aid.  Returns the previous
     setting."""
     return int(load().pkv_testing_set_decode_wait_limit(int(tries)))
+
+
+def pkv_testing_set_shared_prefix_path(path):
+    """Route of later shared-prefix decode calls (0: the library's choice,
+    1: the single pass, 2: prefix kernel + partitions + reduce); a testing
+    aid.  Returns the previous setting."""
+    r = int(load().pkv_testing_set_shared_prefix_path(int(path)))
+    if r < 0:
+        raise ValueError("path must be 0, 1 or 2")
+    return r
 
 
 def pkv_shared_prefix_workspace_bytes(cache, num_seqs, num_heads, max_context_len,

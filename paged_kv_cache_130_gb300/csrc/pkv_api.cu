@@ -88,7 +88,8 @@ int device_sms()
         return 152;
     int v = cache[dev].load(std::memory_order_relaxed);
     if (v <= 0) {
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            v <= 0)
             return 152;
         cache[dev].store(v, std::memory_order_relaxed);
     }
@@ -303,6 +304,14 @@ pkv_status check_workspace(const WorkspaceLayout& wl, const void* workspace, siz
 // The wait limit that pkv_testing_set_decode_wait_limit sets (0 = the
 // kernels' own).
 std::atomic<uint32_t> g_decode_wait_tries{0};
+// The shared-prefix path that pkv_testing_set_shared_prefix_path sets.
+std::atomic<int32_t> g_shared_prefix_path{0};
+
+// Longest context the single-pass shared-prefix decode takes by itself: one
+// CTA streams the prefix and every member's own blocks of its row tile, so
+// its work grows with the contexts; beyond this the split path balances
+// better.
+constexpr int32_t kGroupMaxContext = 4096;
 
 }  // namespace
 
@@ -311,11 +320,23 @@ uint32_t pkv::decode_wait_tries()
     return g_decode_wait_tries.load(std::memory_order_relaxed);
 }
 
+int32_t pkv::shared_prefix_path()
+{
+    return g_shared_prefix_path.load(std::memory_order_relaxed);
+}
+
 extern "C" {
 
 uint32_t pkv_testing_set_decode_wait_limit(uint32_t tries)
 {
     return g_decode_wait_tries.exchange(tries, std::memory_order_relaxed);
+}
+
+int32_t pkv_testing_set_shared_prefix_path(int32_t path)
+{
+    if (path < 0 || path > 2)
+        return -1;
+    return g_shared_prefix_path.exchange(path, std::memory_order_relaxed);
 }
 
 
@@ -564,6 +585,26 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
     if (st != PKV_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (prefixes) {
+        // Single pass (one CTA per group, KV head and row tile; no partials)
+        // when the library chooses the split (partition_size 0), the contexts
+        // are short enough for one CTA to stream a tile's members, and the
+        // CTAs cover the GPU at least once.
+        const pkv::DecodeParams p =
+            decode_params(cache, q, q_dtype, num_seqs, num_heads, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, part,
+                          workspace, wl, grp, dev_err, out);
+        const int32_t path = pkv::shared_prefix_path();
+        const bool single = path == 1 ||
+                            (path == 0 && partition_size == 0 &&
+                             max_context_len <= kGroupMaxContext &&
+                             pkv::group_decode_ctas(p) >= device_sms());
+        if (single) {
+            const cudaError_t e = pkv::launch_decode_group(p, s);
+            if (e != cudaErrorNotSupported)
+                return from_cuda(e);
+        }
+    }
     if (prefixes) {
         const pkv::DecodeParams p =
             decode_params(cache, q, q_dtype, num_seqs, num_heads, block_tables,

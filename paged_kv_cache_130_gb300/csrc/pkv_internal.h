@@ -195,6 +195,16 @@ cudaError_t launch_decode_stream(const DecodeParams& p, bool mma, cudaStream_t s
 cudaError_t launch_decode_prefix(const DecodeParams& p, cudaStream_t stream);
 bool prefix_kernel_supported(int cache_dtype, int q_dtype, int head_dim, int block_size,
                              int group);
+// Single-pass shared-prefix decode (decode_group.cu): one CTA per (group, KV
+// head, row tile) reads the shared blocks once and each member's own blocks,
+// and writes out directly (no partials, no reduce).  Same shapes as the
+// prefix kernel; NotSupported when the cache is too large for a tensor map.
+cudaError_t launch_decode_group(const DecodeParams& p, cudaStream_t stream);
+int64_t group_decode_ctas(const DecodeParams& p);
+// Which shared-prefix path the calls take: 0 = the library's choice, 1 = the
+// single pass, 2 = prefix kernel + partition kernel + reduce
+// (pkv_testing_set_shared_prefix_path).
+int32_t shared_prefix_path();
 cudaError_t launch_lse_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);

@@ -5,7 +5,12 @@ blocks by reference (ã€ŒKV ç¼“å­˜ä¸åˆ†é¡µæ³¨æ„åŠ›ã€ Â§08 å…±ç”¨ï¼Œå†™æ—¶å¤åˆ
 entry point reads those blocks once per group and splits each context at the
 end of the shared prefix; the attention it returns is the same exact
 attention, so the oracle's plain decode is the reference:
-|gpu - oracle| <= 2e-3 + 2e-3 |oracle| (plus half an ulp of the output type).
+|gpu - oracle| <= 2e-3 + 2e-3 |oracle| (plus half a bf16 ulp for bf16 outputs).
+
+The entry point has two routes, and every case runs through both: the single
+pass (one kernel reads a group's shared blocks once for all its rows, then
+each member's own blocks, and writes out) and the split (prefix kernel,
+partition kernel over the rest of each context, log-sum-exp reduce).
 """
 import numpy as np
 import pytest
@@ -22,6 +27,19 @@ pytestmark = pytest.mark.gpu
 def _lib():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     H.build_library()
+    yield
+    B.pkv_testing_set_shared_prefix_path(0)
+
+
+PATHS = {"single_pass": 1, "split": 2}
+
+
+@pytest.fixture(params=list(PATHS))
+def route(request):
+    """The shared-prefix route the test's calls take."""
+    prev = B.pkv_testing_set_shared_prefix_path(PATHS[request.param])
+    yield request.param
+    B.pkv_testing_set_shared_prefix_path(prev)
 
 
 def forked(**kw):
@@ -57,7 +75,7 @@ CASES = {
 
 
 @pytest.mark.parametrize("case", list(CASES))
-def test_shared_prefix_matches_oracle(case):
+def test_shared_prefix_matches_oracle(case, route):
     kw, ps = CASES[case]
     w = forked(**kw)
     begin, blocks = w.prefix_groups()
@@ -66,7 +84,7 @@ def test_shared_prefix_matches_oracle(case):
     out = g.decode_shared(partition_size=ps)
     ref = o.decode()
     torch.cuda.synchronize()
-    H.assert_attention_close(H.out_to_double(out), ref, case, w.io_dtype)
+    H.assert_attention_close(H.out_to_double(out), ref, case + " " + route, w.io_dtype)
     assert int(g.dev_err.item()) == 0
     # the plain decode of the same batch agrees too
     out2 = g.decode(partition_size=ps)
@@ -75,17 +93,31 @@ def test_shared_prefix_matches_oracle(case):
 
 
 def test_full_size_cow_layer():
+    """The parallel-sampling layer at full size on the library's own route
+    (the single pass, as the benchmark runs it), sampled rows against the
+    oracle, and the split route agreeing with it everywhere."""
     w = W.cow_parallel_sampling_f16()
     g, o = prepared(w)
-    out = g.decode_shared()
+    out = g.decode_shared().clone()
     torch.cuda.synchronize()
     seqs = [0, 5, 6, 47, 90, 95]
     ref = o.decode(seqs)
     H.assert_attention_close(H.out_to_double(out)[seqs], ref, "cow full", w.io_dtype)
     assert int(g.dev_err.item()) == 0
+    prev = B.pkv_testing_set_shared_prefix_path(2)
+    try:
+        split = g.decode_shared()
+        torch.cuda.synchronize()
+    finally:
+        B.pkv_testing_set_shared_prefix_path(prev)
+    # both routes are within 2e-3 + 2e-3 |ref| of the exact result; between
+    # them, twice that
+    a, b = H.out_to_double(out), H.out_to_double(split)
+    assert np.all(np.abs(a - b) <= 2 * (H.ATOL + H.RTOL * np.abs(b)))
+    assert int(g.dev_err.item()) == 0
 
 
-def test_whole_context_shared_and_singletons():
+def test_whole_context_shared_and_singletons(route):
     """A member whose context is exactly the prefix (nothing after it), groups
     of one, and a group whose entry says 0 blocks."""
     w = forked(num_heads=8, prompt_len=64, tail_hi=20)
@@ -110,7 +142,7 @@ def test_whole_context_shared_and_singletons():
     assert int(g.dev_err.item()) == 0
 
 
-def test_bad_group_entries_are_flagged():
+def test_bad_group_entries_are_flagged(route):
     """A prefix longer than a member's context zeroes that member and flags
     PKV_DEVERR_CONTEXT; a member whose table differs inside the prefix flags
     PKV_DEVERR_PREFIX (its output is then not defined: the prefix kernel read
@@ -144,3 +176,45 @@ def test_bad_group_entries_are_flagged():
                     max_group_size=6, max_prefix_blocks=4)
     torch.cuda.synchronize()
     assert int(g.dev_err.item()) & B.PKV_DEVERR_PREFIX
+
+
+def test_unusable_group_entry_zeroes_its_members(route):
+    """A group whose prefix count exceeds max_prefix_blocks is flagged and its
+    members' outputs are zero; the other group is unaffected."""
+    w = forked(num_heads=8, prompt_len=64, tail_hi=20)
+    g, o = prepared(w)
+    out = g.decode_shared(groups=(np.array([0, 6, 12], np.int32), np.array([7, 4], np.int32)),
+                          max_group_size=6, max_prefix_blocks=5)
+    torch.cuda.synchronize()
+    err = int(g.dev_err.item())
+    assert err & B.PKV_DEVERR_PREFIX and err & B.PKV_DEVERR_CONTEXT
+    got = out.float().cpu()
+    assert torch.all(got[:6] == 0)
+    ref = o.decode(list(range(6, 12)))
+    H.assert_attention_close(got[6:12].double().numpy(), ref, "good group " + route, w.io_dtype)
+
+
+def test_single_pass_wait_that_runs_out_is_flagged():
+    """The single pass's bounded waits: with one poll per wait a wait runs
+    out, PKV_DEVERR_TIMEOUT is set and the kernel returns; the next call, with
+    the kernel's own limit, is correct."""
+    w = forked(num_prompts=3)
+    g, o = prepared(w)
+    ref = o.decode()
+    prev_path = B.pkv_testing_set_shared_prefix_path(1)
+    prev = B.pkv_testing_set_decode_wait_limit(1)
+    try:
+        g.decode_shared()
+        torch.cuda.synchronize()
+        assert int(g.dev_err.item()) & B.PKV_DEVERR_TIMEOUT
+    finally:
+        B.pkv_testing_set_decode_wait_limit(prev)
+    try:
+        g.dev_err.zero_()
+        out = g.decode_shared()
+        torch.cuda.synchronize()
+    finally:
+        B.pkv_testing_set_shared_prefix_path(prev_path)
+    assert int(g.dev_err.item()) == 0
+    H.assert_attention_close(H.out_to_double(out), ref, "single pass after a time-out",
+                             w.io_dtype)
