@@ -97,11 +97,18 @@ __device__ __forceinline__ float2 unpack2<kBF16>(uint32_t w)
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Two E4M3 codes (low byte = element 0) to float, through the hardware
-// e4m3x2 -> f16x2 conversion (exact: every E4M3 value is an fp16 value).
-__device__ __forceinline__ float2 unpack_e4m3x2(uint16_t w)
+// Four E4M3 codes (byte i = element i) -> two f16 pairs (elements 0, 1 and
+// 2, 3), each exact; the conversions read the word's 16-bit halves directly.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w), __NV_E4M3);
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
+        " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h)
+{
     __half2 hh = *reinterpret_cast<__half2*>(&h);
     return __half22float2(hh);
 }
@@ -114,8 +121,10 @@ __device__ __forceinline__ void unpack_vec(const uint4& v, float* out)
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float2 a = unpack_e4m3x2(static_cast<uint16_t>(w[i] & 0xffffu));
-            float2 b = unpack_e4m3x2(static_cast<uint16_t>(w[i] >> 16));
+            uint32_t lo, hi;
+            e4m3x4_to_f16x2(w[i], lo, hi);
+            const float2 a = f16x2_to_float2(lo);
+            const float2 b = f16x2_to_float2(hi);
             out[4 * i + 0] = a.x;
             out[4 * i + 1] = a.y;
             out[4 * i + 2] = b.x;
