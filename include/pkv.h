@@ -180,6 +180,23 @@ pkv_status pkv_swap_blocks(const pkv_cache_desc* src, const pkv_cache_desc* dst,
                            int32_t* dev_err, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * pkv_testing_stream_copy -- a measurement aid, not part of the method (the
+ * pages have no counterpart).
+ *
+ * Copies `bytes` (a multiple of 16) from src to dst with plain SM loads and
+ * stores, many 16-byte vectors in flight per thread, as a reference for what
+ * a copy kernel can reach over a given link: between device memory and
+ * pinned, device-mapped host memory it shows the NVLink-C2C rate that SMs
+ * see, which pkv_swap_blocks is measured against (the copy engines'
+ * cudaMemcpyAsync rate is a different path).  Both pointers must be 16-byte
+ * aligned and reachable by the GPU (device memory, or pinned host memory;
+ * checked with cudaPointerGetAttributes, else PKV_ERR_INVALID_ARG before any
+ * launch).  The ranges must not overlap.  Asynchronous on `stream`.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_testing_stream_copy(void* dst, const void* src, int64_t bytes,
+                                   pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Block hashes for prefix caching -- every full block gets a hash of its
  * tokens and of all the content in front of it, so that requests with the same
  * opening find the same blocks (「KV 缓存与分页注意力」 §11; 「KV Cache从原理到实战」

@@ -84,6 +84,7 @@ def load():
                                                            vp, ctypes.c_size_t, vp, vp, vp]),
         "pkv_testing_set_decode_wait_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
         "pkv_testing_set_shared_prefix_path": (i32, [i32]),
+        "pkv_testing_stream_copy": (i32, [vp, vp, i64, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -355,6 +356,17 @@ def pkv_swap_blocks(src, dst, block_pairs, dev_err=None, stream=None):
         raise ValueError("block_pairs must be int64 [n, 2]")
     _check(load().pkv_swap_blocks(a, b, len(src), _ptr(block_pairs), block_pairs.numel() // 2,
                                   _ptr(dev_err), _stream(stream)), "pkv_swap_blocks")
+
+
+def pkv_testing_stream_copy(dst, src, stream=None):
+    """Copy src into dst (same byte size) with SM loads and stores: the
+    measurement reference for copies over a link (device <-> pinned host)."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src must have the same byte size")
+    _check(load().pkv_testing_stream_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)),
+           "pkv_testing_stream_copy")
+    return dst
 
 
 def pkv_block_hashes(token_ids, cu_seqlens, block_size, block_offsets=None, parent_hashes=None,

@@ -741,6 +741,20 @@ pkv_status pkv_swap_blocks(const pkv_cache_desc* src, const pkv_cache_desc* dst,
     return PKV_OK;
 }
 
+pkv_status pkv_testing_stream_copy(void* dst, const void* src, int64_t bytes,
+                                   pkv_stream_t stream)
+{
+    if (bytes < 0 || bytes % 16 != 0 || !aligned16(dst) || !aligned16(src))
+        return PKV_ERR_INVALID_ARG;
+    if (bytes == 0)
+        return PKV_OK;
+    void* d = nullptr;
+    void* s = nullptr;
+    if (!device_reachable(dst, &d) || !device_reachable(src, &s))
+        return PKV_ERR_INVALID_ARG;
+    return from_cuda(pkv::launch_stream_copy(d, s, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_block_hashes(const int32_t* token_ids, const int32_t* cu_seqlens,
                             int32_t num_seqs, int64_t total_tokens, int32_t block_size,
                             const uint8_t* parent_hashes, const int64_t* block_offsets,

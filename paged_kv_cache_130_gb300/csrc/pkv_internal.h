@@ -162,6 +162,8 @@ struct SwapParams {
 };
 
 cudaError_t launch_swap_blocks(const SwapParams& p, cudaStream_t stream);
+// Streaming copy of `bytes` (a multiple of 16) with SM loads and stores.
+cudaError_t launch_stream_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream);
 
 // SHA-256 constants (FIPS 180-4 §4.2.2, §5.3.3), derived on the host.
 struct Sha256Table {

@@ -52,7 +52,57 @@ __global__ void __launch_bounds__(kSwapThreads) swap_blocks_kernel(const SwapPar
     }
 }
 
+// A plain streaming copy with SM loads and stores: every thread moves
+// kProbeVec 16-byte vectors per round (all loads before the stores), rounds
+// striding over the whole grid.  It measures what SMs reach over a link (for
+// instance device memory <-> pinned host memory over NVLink-C2C), the ceiling
+// a copy kernel such as swap_blocks_kernel can aim for.
+constexpr int kProbeThreads = 256;
+constexpr int kProbeVec = 8;
+
+__global__ void __launch_bounds__(kProbeThreads) stream_copy_kernel(uint4* dst, const uint4* src,
+                                                                    int64_t n16)
+{
+    const int64_t stride = (int64_t)gridDim.x * kProbeThreads * kProbeVec;
+    for (int64_t base = (int64_t)blockIdx.x * kProbeThreads * kProbeVec; base < n16;
+         base += stride) {
+        uint4 buf[kProbeVec];
+#pragma unroll
+        for (int j = 0; j < kProbeVec; ++j) {
+            const int64_t i = base + (int64_t)j * kProbeThreads + threadIdx.x;
+            if (i < n16)
+                buf[j] = src[i];
+        }
+#pragma unroll
+        for (int j = 0; j < kProbeVec; ++j) {
+            const int64_t i = base + (int64_t)j * kProbeThreads + threadIdx.x;
+            if (i < n16)
+                dst[i] = buf[j];
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_stream_copy(void* dst, const void* src, int64_t bytes, cudaStream_t stream)
+{
+    if (bytes <= 0)
+        return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t n16 = bytes / 16;
+    const int64_t per_cta = (int64_t)kProbeThreads * kProbeVec;
+    int64_t ctas = (n16 + per_cta - 1) / per_cta;
+    if (ctas > 4LL * sms)
+        ctas = 4LL * sms;
+    stream_copy_kernel<<<(unsigned)ctas, kProbeThreads, 0, stream>>>(
+        reinterpret_cast<uint4*>(dst), reinterpret_cast<const uint4*>(src), n16);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_swap_blocks(const SwapParams& p, cudaStream_t stream)
 {

@@ -89,3 +89,25 @@ def test_swap_between_device_pools_and_bad_pairs():
     want[5] = src[9]
     want[1] = src[1]
     assert np.array_equal(got, want)
+
+
+def test_stream_copy_moves_bytes_both_ways():
+    """The SM streaming copy the swap bench measures the link with: device to
+    pinned host and back, byte for byte, a size that is not a multiple of the
+    grid's round; a misaligned pointer or size is refused."""
+    rng = np.random.default_rng(11)
+    n = (3 << 20) + 48
+    src = torch.from_numpy(rng.integers(0, 256, size=n, dtype=np.uint8)).cuda()
+    host = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    back = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    B.pkv_testing_stream_copy(host, src)
+    torch.cuda.synchronize()
+    assert torch.equal(host, src.cpu())
+    B.pkv_testing_stream_copy(back, host)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    lib = B.load()
+    st = lib.pkv_testing_stream_copy(B._ptr(back[1:]), B._ptr(src[1:]), 16, None)
+    assert st == B.PKV_ERR_INVALID_ARG
+    st = lib.pkv_testing_stream_copy(B._ptr(back), B._ptr(src), 24, None)
+    assert st == B.PKV_ERR_INVALID_ARG
