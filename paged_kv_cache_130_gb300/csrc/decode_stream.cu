@@ -276,7 +276,8 @@ constexpr int kMaxUnitParts = 4;
 constexpr int kSchedSlots = 1024;     // launches that may be in flight at once
 
 // Dynamic work distribution.  Slot k serves one launch: [0] hands out the next
-// work item, [1] counts the CTAs that have stopped taking items.  The array is
+// work unit after the first gridDim.x (CTA c takes unit c without a claim),
+// [1] counts the CTAs that have stopped taking units.  The array is
 // zero when the module loads, and the CTA that stops last resets its slot to
 // zero, so every launch finds its slot at zero as long as fewer than
 // kSchedSlots launches run at the same time.
@@ -521,15 +522,21 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
         uint32_t armed = 0;          // one past the last tile whose copies started
         int published = 0;
         bool stop = false;
-        for (;;) {
+        for (bool first = true;; first = false) {
             // one claim hands out a unit: unit_parts consecutive partitions
             // of one (sequence, query head), streamed back to back so that
-            // the claim's and the block table's round trips are paid once
+            // the claim's and the block table's round trips are paid once.
+            // A CTA's first unit is its own index (no round trip before its
+            // first table read); the counter hands out the rest from
+            // gridDim.x on.
             int unit = 0;
-            if (lane == 0) {
-                unit = (int)atomicAdd(&g_sched[slot][0], 1u);
-                // one launch hands out at most num_items + gridDim.x claims:
-                // a higher count means another launch shares the slot
+            if (first) {
+                unit = (int)blockIdx.x;
+            } else if (lane == 0) {
+                unit = (int)(atomicAdd(&g_sched[slot][0], 1u) + gridDim.x);
+                // the counter serves num_items - gridDim.x units and one
+                // failed claim per CTA, so unit < num_items + gridDim.x: a
+                // higher one means another launch shares the slot
                 if ((unsigned)unit >= (unsigned)num_items + gridDim.x)
                     flag_error(p.dev_err, PKV_DEVERR_SCHED);
             }
