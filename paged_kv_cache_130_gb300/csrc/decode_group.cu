@@ -260,6 +260,7 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
         *armed_rec = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
     // launched with programmatic dependent launch: read nothing before the
     // preceding kernel in the stream is complete
     pdl_wait_primary();
@@ -295,9 +296,11 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
     it.prefix = blocks * BS;
     it.row0 = tile * RT;
     it.nrows = min(RT, it.nmem * G - it.row0);
-    if (tile == 0) {
+    // the producer warp starts streaming as soon as the item is known; the
+    // consumers do the checks and load q meanwhile
+    if (tile == 0 && warp < kNC) {
         // members past max_group_size have no tile: zero their rows
-        for (int i = threadIdx.x; i < (b1 - it.b0 - it.nmem) * G * D; i += blockDim.x) {
+        for (int i = threadIdx.x; i < (b1 - it.b0 - it.nmem) * G * D; i += kNC * 32) {
             const int m = it.nmem + i / (G * D);
             const int h = it.g * G + (i / D) % G;
             if (i % (G * D) == 0)
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
         // every member's table must hold the first member's prefix blocks
         if (it.g == 0) {
             const int32_t* lead = p.block_tables + (int64_t)it.b0 * p.max_blocks_per_seq;
-            for (int i = threadIdx.x; i < (it.nmem - 1) * blocks; i += blockDim.x) {
+            for (int i = threadIdx.x; i < (it.nmem - 1) * blocks; i += kNC * 32) {
                 const int m = 1 + i / blocks;
                 const int b = i % blocks;
                 if (__ldg(lead + (int64_t)m * p.max_blocks_per_seq + b) != __ldg(lead + b))
@@ -329,8 +332,8 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
 
     // Q^T fragments (rows gq, gq + 8 of the n-tiles; zero past nrows), each
     // lane reading back its own 16 bytes; lane t of a quad holds chunk
-    // kchunk(i, t) of k-slice i, as for K
-    for (int i = threadIdx.x; i < NNT * NS * 32; i += blockDim.x) {
+    // kchunk(i, t) of k-slice i, as for K (consumer threads only)
+    for (int i = threadIdx.x; warp < kNC && i < NNT * NS * 32; i += kNC * 32) {
         const int ln = i & 31;
         const int r = (ln >> 2) + 8 * (i / (NS * 32));
         const int sl = (i >> 5) % NS;
@@ -342,17 +345,17 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
         }
         sq[i] = v;
     }
-    __syncthreads();
 
     if (warp == kNC) {
         // ------------------------------------------------------------ producer
         uint32_t tt = 0;
         bool stop = false;
-        // the first 32 table entries of a segment, one per lane; read one
-        // segment ahead, so that the round trips of the next member's context
-        // length and table overlap this segment's copies
+        // the first 32 table entries of a segment, one per lane, read before
+        // (and without waiting for) the member's context length -- entries
+        // past the context are read but not used -- and one segment ahead, so
+        // that these round trips overlap the copies before them
         auto first_chunk = [&](const Segment& sg) -> int {
-            const int n = min(32, sg.blk1 - sg.blk0);
+            const int n = min(32, p.max_blocks_per_seq - sg.blk0);
             return lane < n ? __ldg(sg.table + sg.blk0 + lane) : -1;
         };
         Segment sg = segment<BS>(p, it, 0, nseg);
@@ -414,6 +417,7 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
         }
     } else {
         // ------------------------------------------------------------ consumers
+        consumers_sync();                       // q fragments are in shared memory
         // tiles of the whole stream, counted the producer's way
         uint32_t ntile = 0;
         for (int k = 0; k < nseg; ++k) {
