@@ -42,34 +42,40 @@ MODEL_LAYERS = {"opt13b_f16": 40, "llama2_70b_bf16_gqa": 80, "llama2_7b_fp8_long
                 "cow_parallel_sampling_f16": 40, "tiny_f16": 1}
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes per launch of the decode partition kernel from an ncu capture,
-# valid while the decode kernel and partition-rule sources hash to "src_sha"
-# (else reported as null)
+# DRAM bytes (read + write) per launch of the timed kernel from a one-pass ncu
+# capture (dram__bytes_read.sum, dram__bytes_write.sum, gpu__time_duration.sum)
+# of the full-size workload, valid while the sources hash to "src_sha" (else
+# reported as null); "profile" names the summary under profiles/ that prints
+# the figures and the command.
 NCU_TRAFFIC = {
-    "opt13b_f16": {"bytes_per_launch": 366095360 + 3499264, "src_sha": "dfa23bf00e5141bb"},
-    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642880000 + 3004160,
-                            "src_sha": "dfa23bf00e5141bb"},
-    # one-pass capture (dram bytes and duration only) on the full-size workload
-    "llama2_7b_fp8_long": {"bytes_per_launch": 2498218496 + 13027072,
-                           "src_sha": "dfa23bf00e5141bb"},
-    # prefix kernel + partition kernel of one shared-prefix decode call
+    "opt13b_f16": {"bytes_per_launch": 366086912 + 3072256, "src_sha": "d3ce772ce427fdef",
+                   "profile": "profiles/decode_stream_kernel_opt13b_f16.md"},
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642887680 + 2719232,
+                            "src_sha": "d3ce772ce427fdef",
+                            "profile": "profiles/decode_mma_kernel_llama2_70b_bf16_gqa.md"},
+    "llama2_7b_fp8_long": {"bytes_per_launch": 2498331648 + 12674048,
+                           "src_sha": "d3ce772ce427fdef",
+                           "profile": "profiles/decode_stream_kernel_llama2_7b_fp8_long.md"},
+    # the single-pass shared-prefix kernel (the whole decode call)
     "cow_parallel_sampling_f16:shared-prefix": {
-        "bytes_per_launch": 130871552 + 2943488 + 251801344 + 1080832,
-        "src_sha": "dfa23bf00e5141bb"},
+        "bytes_per_launch": 381784832 + 2971136, "src_sha": "d3ce772ce427fdef",
+        "profile": "profiles/decode_group_kernel_cow_parallel_sampling_f16.md"},
 }
-DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_common.cuh", "pkv_common.cuh",
-                  "pkv_api.cu")
-# the same for the prefill kernel (DRAM bytes of one launch)
+DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_group.cu", "decode_common.cuh",
+                  "pkv_common.cuh", "pkv_api.cu")
+# the same for the prefill kernel
 NCU_PREFILL_TRAFFIC = {
-    "prefill_llama2_7b_bf16": {"bytes_per_launch": 646965248 + 71444992,
-                               "src_sha": "a635cf156331c4ca"},
-    # one-pass capture (DRAM bytes and duration only)
-    "prefill_llama2_70b_gqa_chunked_bf16": {"bytes_per_launch": 181151488 + 29108480,
-                                            "src_sha": "a635cf156331c4ca"},
+    "prefill_llama2_7b_bf16": {"bytes_per_launch": 647137536 + 71322112,
+                               "src_sha": "0ba540cc6e5325c3",
+                               "profile": "profiles/prefill_ws_kernel_prefill_llama2_7b_bf16.md"},
+    "prefill_llama2_70b_gqa_chunked_bf16": {
+        "bytes_per_launch": 183102464 + 29753600, "src_sha": "0ba540cc6e5325c3",
+        "profile": "profiles/prefill_ws_kernel_prefill_llama2_7b_bf16.md"},
 }
 # the same for the block-hash kernel
 NCU_HASH_TRAFFIC = {
-    "hash_prompts": {"bytes_per_launch": 21091072 + 0, "src_sha": "3ecb8b33a5490a6c"},
+    "hash_prompts": {"bytes_per_launch": 21091328 + 0, "src_sha": "e776a2cab7bb853f",
+                     "profile": "profiles/block_hash_kernel_hash_prompts.md"},
 }
 HASH_SOURCES = ("block_hash.cu", "pkv_common.cuh")
 PREFILL_SOURCES = ("prefill_ws.cu", "tc_common.cuh", "pkv_common.cuh")

@@ -68,3 +68,27 @@ def test_config_summary_and_options():
     assert bench.parse_args(["--configs", "none"]).configs == "none"
     assert set(bench.EXTRA_CONFIGS) == {"llama2_70b_bf16_gqa", "cow_parallel_sampling_f16",
                                         "llama2_7b_fp8_long"}
+
+
+def test_every_ncu_traffic_figure_is_in_its_profile():
+    """Each DRAM-traffic constant bench.py reports names a tracked summary
+    under profiles/ that prints both byte counts and the source hash the
+    constant is valid for."""
+    import os
+    tables = [bench.NCU_TRAFFIC, bench.NCU_PREFILL_TRAFFIC, bench.NCU_HASH_TRAFFIC]
+    for table in tables:
+        for name, tr in table.items():
+            path = os.path.join(bench.ROOT, tr["profile"])
+            assert os.path.exists(path), (name, path)
+            text = open(path).read().replace(",", "")
+            assert tr["src_sha"] in text, (name, "source hash missing")
+            # the constant is read + write from the capture, both printed
+            found = any(int(a) + int(b) == tr["bytes_per_launch"]
+                        for a in __import__("re").findall(r"(\d{6,})", text)
+                        for b in __import__("re").findall(r"(\d+) B", text))
+            assert found, (name, "byte counts missing")
+    # and the hashes are those of the current sources
+    assert bench.NCU_TRAFFIC["opt13b_f16"]["src_sha"] == bench.decode_src_sha()
+    assert bench.NCU_PREFILL_TRAFFIC["prefill_llama2_7b_bf16"]["src_sha"] == \
+        bench.src_sha(bench.PREFILL_SOURCES)
+    assert bench.NCU_HASH_TRAFFIC["hash_prompts"]["src_sha"] == bench.src_sha(bench.HASH_SOURCES)
