@@ -386,6 +386,33 @@ def workload_config(w):
             "parallelism": "replicas"}
 
 
+def step_graph(stream, stages):
+    """The stages of one step captured into ONE CUDA graph, with an event node
+    before the first stage and after each, so that each stage is timed inside
+    the step as an engine that captures its whole step runs it (no graph
+    launch between stages).  Returns a function that replays the graph, waits
+    for it and returns each stage's milliseconds; None where this PyTorch
+    cannot record timing events inside a capture."""
+    import torch
+    try:
+        evs = [torch.cuda.Event(enable_timing=True, external=True)
+               for _ in range(len(stages) + 1)]
+    except TypeError:
+        return None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        evs[0].record()
+        for i, fn in enumerate(stages):
+            fn()
+            evs[i + 1].record()
+
+    def run():
+        g.replay()
+        evs[-1].synchronize()
+        return [evs[i].elapsed_time(evs[i + 1]) for i in range(len(stages))]
+    return run
+
+
 def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
     """Time the decode step of workload `w` on this rank's GPU; returns the
     JSON line (rank 0) or None.  The cache is filled from the workload's
@@ -559,8 +586,28 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
         b.record()
         torch.cuda.synchronize()
         part_ms = [a.elapsed_time(b) / args.steps] * args.steps
+
+    # the step again as ONE graph (copy, append and decode captured
+    # together, event nodes between them): the decode call's interval then
+    # holds no graph launch, as in an engine that captures its whole step
+    one_graph = None
+    timer = step_graph(stream, [pre, decode]) if not args.no_graphs else None
+    if timer is not None:
+        for i in range(args.warmup):
+            maybe_flush(i)
+            timer()
+        one_graph = []
+        for i in range(args.steps):
+            maybe_flush(i)
+            one_graph.append(timer())
     clk = clocks.stop() if clocks else None
 
+    # two graphs per step (the copy-and-append graph, then the decode graph)
+    sep_dec_s, sep_step_s = slowest([sum(dec_ms) / 1e3, sum(step_ms) / 1e3], dev)
+    if one_graph is not None:
+        pre_ms = [a for a, _ in one_graph]
+        dec_ms = [b for _, b in one_graph]
+        step_ms = [a + b for a, b in one_graph]
     dec_s = sum(dec_ms) / 1e3
     step_s = sum(step_ms) / 1e3
     dbytes = w.decode_bytes()
@@ -680,8 +727,12 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
     cfg["l2"] = ("decode inputs (%.0f MB of K/V per step) exceed the 129 MB L2; no flush"
                  % (w.kv_bytes() / 1e6) if args.flush == "none"
                  else "512 MiB written between steps (L2 flush)")
-    cfg["timing"] = ("value: CUDA events around CUDA-graph replays of the decode call; "
-                     "roofline: the partition kernel launched `steps` times back to back "
+    cfg["timing"] = (("value: the decode call between event nodes inside one CUDA graph of "
+                      "the whole step (copy, append, decode); separate_graphs: the same "
+                      "with the step as two graphs, events between their replays; "
+                      if one_graph is not None else
+                      "value: CUDA events around CUDA-graph replays of the decode call; ")
+                     + "roofline: the partition kernel launched `steps` times back to back "
                      "between one pair of events; e2e: see e2e.timing") \
         if not args.no_graphs else "CUDA events around direct calls"
     cfg["partition_size"] = ps
@@ -702,6 +753,10 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
             "step_ms": {"copy_and_append": statistics.mean(pre_ms),
                         "decode": statistics.mean(dec_ms), "step": statistics.mean(step_ms)},
             "decode_ms_spread": percentiles(dec_ms),
+            "separate_graphs": {"value": whole_job_rate(rbytes * args.steps, sep_dec_s,
+                                                        world) / 1e9,
+                                "decode_ms": sep_dec_s * 1e3 / args.steps,
+                                "step_ms": sep_step_s * 1e3 / args.steps},
             "decode_bytes": dbytes, "unique_kv_bytes": w.unique_kv_bytes(),
             "roofline": roofline, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

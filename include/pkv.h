@@ -17,7 +17,10 @@
  * Conventions shared by every call
  * --------------------------------
  * Ownership.  The caller owns every buffer.  The library never allocates,
- *   frees or synchronises, and it is thread-safe.  Between calls it keeps only
+ *   frees or synchronises, and it is thread-safe.  A pkv_cache_desc holds
+ *   raw pointers and no reference: the caches it names must stay allocated
+ *   (and mapped) for as long as any call that uses the descriptor may run,
+ *   including every replay of a CUDA graph that captured such a call.  Between calls it keeps only
  *   a per-device record of each decode kernel's launch size and a static
  *   device table of work counters for the streaming decode kernel (the
  *   single-head and FP8 decode): 1024 slots, each reset to zero by the last

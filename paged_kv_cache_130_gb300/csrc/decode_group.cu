@@ -130,13 +130,16 @@ __device__ __forceinline__ void consumers_sync()
 }
 
 // Bounded wait for phase `parity` of the mbarrier at `bar`: false when the CTA
-// gives up (a time-out here, or one elsewhere in the CTA).
+// gives up (a time-out here, or one elsewhere in the CTA).  Under a limit
+// lowered for testing a poll is one non-suspending look (test_wait), so that a
+// one-poll wait that is not already complete always runs out.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag, int32_t* dev_err,
                                               uint32_t tries)
 {
+    const bool look = tries < tc::kSpin;
     for (uint32_t i = 0; i < tries; ++i) {
-        if (tc::try_wait(bar, parity))
+        if (look ? tc::test_wait(bar, parity) : tc::try_wait(bar, parity))
             return true;
         if (*abort_flag)
             return false;
@@ -350,6 +353,8 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
         // ------------------------------------------------------------ producer
         uint32_t tt = 0;
         bool stop = false;
+        // K/V tiles are read once per call: first out of L2
+        const uint64_t kv_policy = l2_evict_first_policy();
         // the first 32 table entries of a segment, one per lane, read before
         // (and without waiting for) the member's context length -- entries
         // past the context are read but not used -- and one segment ahead, so
@@ -394,9 +399,10 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
                                 const int y = (int)(((int64_t)phys * p.num_kv_heads + it.g) * BS);
 #pragma unroll
                                 for (int pn = 0; pn < S::PANELS; ++pn) {
-                                    tc::tma_box(dst + pn * S::PANEL, &tmk, pn * 64, y, fb);
-                                    tc::tma_box(dst + S::TILE + pn * S::PANEL, &tmv, pn * 64, y,
-                                                fb);
+                                    tc::tma_box_hint(dst + pn * S::PANEL, &tmk, pn * 64, y, fb,
+                                                     kv_policy);
+                                    tc::tma_box_hint(dst + S::TILE + pn * S::PANEL, &tmv, pn * 64,
+                                                     y, fb, kv_policy);
                                 }
                             } else {
                                 flag_error(p.dev_err, PKV_DEVERR_BLOCK_ID);

@@ -76,6 +76,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return done != 0;
 }
 
+// The same test without suspending: one look at the phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // global -> shared bulk copy, completion counted in bytes on `bar`
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
 {
@@ -83,6 +97,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
             "r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// The same with an L2 cache policy for the lines it reads.
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 
@@ -103,15 +128,19 @@ __device__ __forceinline__ void consumers_sync(int nthreads)
 
 // Bounded wait for phase `parity` of `bar`: at most `tries` polls.  Returns
 // false when the CTA has given up (time-out here or elsewhere); the caller then
-// skips the stage.
+// skips the stage.  A poll is a try_wait, which may suspend the thread for a
+// while of the hardware's choosing; under a limit lowered for testing it is a
+// test_wait instead, one look, so that a one-poll wait that is not already
+// complete always runs out.
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
                                              volatile int* abort_flag, int32_t* dev_err,
                                              uint32_t tries)
 {
+    const bool look = tries < kSpinLimit;
     for (uint32_t i = 0; i < tries; ++i) {
-        if (mbar_try_wait(bar, parity))
+        if (look ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))
             return true;
         if (*abort_flag)
             return false;
@@ -273,6 +302,13 @@ constexpr int kItemQueue = 4;         // work items the producer may publish ahe
 constexpr int kManyParts = 8;
 constexpr int kUnitTokens = 2048;
 constexpr int kMaxUnitParts = 4;
+// Compact schedule (batches taken longest first, no shared prefixes): units
+// where the sequence has no partition left are not handed out at all, and the
+// last partitions are handed out one at a time, at least kTailUnits per CTA,
+// so that the units the CTAs take last are short.  The schedule is a table of
+// at most kMaxSchedEntries (partition block, unit size) entries.
+constexpr int kTailUnits = 2;
+constexpr int kMaxSchedEntries = 128;
 constexpr int kSchedSlots = 1024;     // launches that may be in flight at once
 
 // Dynamic work distribution.  Slot k serves one launch: [0] hands out the next
@@ -313,8 +349,13 @@ struct StreamSmem {
     static constexpr int drain = abort + 16;
     static constexpr int ctx = drain + 4 * (2 + kItemQueue);
     static constexpr int order = ctx + 4 * kCtxCache;
+    // the compact schedule: partitions per rank, cumulative units per entry,
+    // and [mode, entries, blocks of full units, total units]
+    static constexpr int sched_n = order + 4 * kSortMax;
+    static constexpr int sched_cum = sched_n + 4 * kSortMax;
+    static constexpr int sched_info = sched_cum + 4 * (kMaxSchedEntries + 1);
     static constexpr int QSLOT = ((D * 2 + 127) / 128) * 128;   // q row of one item
-    static constexpr int qbuf = ((order + 4 * kSortMax + 127) / 128) * 128;
+    static constexpr int qbuf = ((sched_info + 16 + 127) / 128) * 128;
     static constexpr int merge_m = qbuf + kItemQueue * QSLOT;
     static constexpr int merge_l = merge_m + 4 * NC;
     static constexpr int merge_acc = merge_l + 4 * NC;
@@ -357,6 +398,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::abort);
     int* sm_ctx = reinterpret_cast<int*>(smem + L::ctx);
     int* sm_order = reinterpret_cast<int*>(smem + L::order);
+    int* sched_n = reinterpret_cast<int*>(smem + L::sched_n);
+    int* sched_cum = reinterpret_cast<int*>(smem + L::sched_cum);
+    int* sched_info = reinterpret_cast<int*>(smem + L::sched_info);
     float* sm_m = reinterpret_cast<float*>(smem + L::merge_m);
     float* sm_l = reinterpret_cast<float*>(smem + L::merge_l);
     float* sm_acc = reinterpret_cast<float*>(smem + L::merge_acc);
@@ -388,6 +432,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
     // end instead)
     if (!p.wait_prior)
         pdl_wait_primary();
+    const int U = p.num_heads;
     const int ncache = min(p.num_seqs, kCtxCache);
     for (int i = threadIdx.x; i < ncache; i += blockDim.x)
         sm_ctx[i] = __ldg(p.context_lens + i);
@@ -408,10 +453,76 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
             sm_order[rank] = i;
         }
     }
+    // The compact schedule, the same in every CTA.  Units go out in the order
+    // (entry, rank, head); entry j < blocks1 is partition block j (unit_parts
+    // partitions from j * unit_parts), each later one a single partition,
+    // and an entry holds only the ranks that have a partition there (with
+    // the ranks ordered longest first these are a prefix of the ranks).
+    if (threadIdx.x == 0)
+        sched_info[0] = 0;
+    const bool try_compact = sorted && unit_parts > 1 &&
+                             (p.grp_begin == nullptr || p.num_groups <= 0);
+    if (try_compact) {
+        __syncthreads();                                   // sm_order complete
+        for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
+            // partitions of rank i's work, as locate_ctx walks them
+            const dec::Split sp = dec::split_context(sm_ctx[sm_order[i]], 0, p.max_context_len,
+                                                     p.partition_size, p.prefix_partition);
+            sched_n[i] = sp.npart <= 1 ? 1 : min(sp.npart, p.grid_partitions);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int ns = p.num_seqs;
+            bool ok = true;
+            for (int i = 1; i < ns; ++i)
+                ok = ok && sched_n[i] <= sched_n[i - 1];
+            const int maxp = sched_n[0];
+            // the first partition of the single-partition tail: the largest
+            // multiple of unit_parts after which at least kTailUnits units a
+            // CTA remain (0: every unit a single partition)
+            int q2 = 0;
+            {
+                int r = 0;
+                int64_t after = 0;
+                for (int q = maxp - 1; q >= 0 && ok; --q) {
+                    while (r < ns && sched_n[r] > q)
+                        ++r;
+                    after += (int64_t)r * U;
+                    if (q % unit_parts == 0 && after >= (int64_t)kTailUnits * gridDim.x) {
+                        q2 = q;
+                        break;
+                    }
+                }
+            }
+            const int blocks1 = q2 / unit_parts;
+            const int entries = blocks1 + (maxp - q2);
+            ok = ok && entries <= kMaxSchedEntries;
+            if (ok) {
+                int r = ns;
+                int64_t cum = 0;
+                sched_cum[0] = 0;
+                for (int j = 0; j < entries && ok; ++j) {
+                    const int q0 = j < blocks1 ? j * unit_parts : q2 + (j - blocks1);
+                    while (r > 0 && sched_n[r - 1] <= q0)
+                        --r;
+                    cum += (int64_t)r * U;
+                    ok = cum <= 0x7fffffffLL;
+                    sched_cum[j + 1] = (int)cum;
+                }
+                if (ok) {
+                    sched_info[1] = entries;
+                    sched_info[2] = blocks1;
+                    sched_info[3] = (int)cum;
+                    sched_info[0] = 1;
+                }
+            }
+        }
+    }
     __syncthreads();
     pdl_launch_dependents();
+    const bool compact = sched_info[0] != 0;
+    const int total_units = compact ? sched_info[3] : num_items;
 
-    const int U = p.num_heads;
     const int64_t block_stride = (int64_t)p.num_kv_heads * TILE;
 
     // -------------------------------------------------------------- consumers
@@ -525,6 +636,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
         // the item queue, then streams its tiles into the ring.
         uint32_t t = 0;
         uint32_t armed = 0;          // one past the last tile whose copies started
+        // K/V tiles are read once per call: first out of L2
+        const uint64_t kv_policy = l2_evict_first_policy();
         int published = 0;
         bool stop = false;
         for (bool first = true;; first = false) {
@@ -539,23 +652,45 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
                 unit = (int)blockIdx.x;
             } else if (lane == 0) {
                 unit = (int)(atomicAdd(&g_sched[slot][0], 1u) + gridDim.x);
-                // the counter serves num_items - gridDim.x units and one
-                // failed claim per CTA, so unit < num_items + gridDim.x: a
+                // the counter serves total_units - gridDim.x units and one
+                // failed claim per CTA, so unit < total_units + gridDim.x: a
                 // higher one means another launch shares the slot
-                if ((unsigned)unit >= (unsigned)num_items + gridDim.x)
+                if ((unsigned)unit >= (unsigned)total_units + gridDim.x)
                     flag_error(p.dev_err, PKV_DEVERR_SCHED);
             }
             unit = __shfl_sync(0xffffffffu, unit, 0);
-            const bool last = unit >= num_items;
-            for (int sub = 0; sub < (last ? 1 : unit_parts); ++sub) {
+            const bool last = unit >= total_units;
+            // the unit's (rank, head, first partition, partitions)
+            int u_rank = 0, u_head = 0, u_q0 = 0, u_parts = unit_parts;
+            if (!last && compact) {
+                int lo = 0;
+                int hi = sched_info[1];          // the entry j with cum[j] <= unit < cum[j + 1]
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (sched_cum[mid] <= unit)
+                        lo = mid;
+                    else
+                        hi = mid;
+                }
+                const int local = unit - sched_cum[lo];
+                u_rank = local / U;
+                u_head = local % U;
+                const int blocks1 = sched_info[2];
+                u_q0 = lo < blocks1 ? lo * unit_parts : blocks1 * unit_parts + (lo - blocks1);
+                u_parts = lo < blocks1 ? unit_parts : 1;
+            } else if (!last) {
+                u_head = unit % U;
+                u_rank = (unit / U) % p.num_seqs;
+                u_q0 = (unit / U / p.num_seqs) * unit_parts;
+            }
+            for (int sub = 0; sub < (last ? 1 : u_parts); ++sub) {
                 int item = -1;
                 int u = 0, s = 0;
                 PartitionWork w{};
                 if (!last) {
-                    u = unit % U;
-                    const int rest = unit / U;
-                    const int rank = rest % p.num_seqs;
-                    const int part = (rest / p.num_seqs) * unit_parts + sub;
+                    u = u_head;
+                    const int rank = u_rank;
+                    const int part = u_q0 + sub;
                     if (part >= p.grid_partitions)
                         break;
                     s = sorted ? sm_order[rank] : rank;
@@ -632,8 +767,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
                             const char* ksrc = kbase + (int64_t)phys * block_stride;
                             const char* vsrc = vbase + (int64_t)phys * block_stride;
                             if (lane == 0) {
-                                bulk_load(dst, ksrc, TILE, &full[stage]);
-                                bulk_load(dst + Shape::VOFF, vsrc, TILE, &full[stage]);
+                                bulk_load_hint(dst, ksrc, TILE, &full[stage], kv_policy);
+                                bulk_load_hint(dst + Shape::VOFF, vsrc, TILE, &full[stage],
+                                               kv_policy);
                             }
                         }
                         ++t;
@@ -798,8 +934,10 @@ cudaError_t stream_simt(const DecodeParams& p, cudaStream_t st)
 }  // namespace
 
 // Streaming decode partitions for single-head work items.  Grouped heads go to
-// the one-CTA-per-item tensor-core kernel (decode.cu): a grouped-head variant
-// of this kernel ended in GPU faults whose cause was not found, and is gone.
+// the one-CTA-per-item tensor-core kernel (decode.cu).  (A grouped-head
+// variant of this kernel ran a ring of 6 stages for 4 consumer warps, the
+// stage-parity race the static_assert on NSTG % NC now rejects, and faulted;
+// it is gone.)
 cudaError_t launch_decode_stream(const DecodeParams& p, bool mma, cudaStream_t stream)
 {
     if (mma)

@@ -25,6 +25,17 @@ struct Elem {
 
 // ------------------------------------------------------------------ loads
 
+// An L2 policy for data read once (K/V tiles, for the bulk and tensor copies
+// that take a cache hint): its lines are the first to go when L2 needs room,
+// so that a stream of them does not push out other lines (such as those an
+// earlier kernel wrote and L2 has not yet written back).
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 16-byte load of data that is read once (K/V tiles): skip L1 allocation.
 __device__ __forceinline__ uint4 ld_stream(const void* p)
 {

@@ -99,6 +99,19 @@ __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// The same test without suspending: one look at the phase.
+__device__ __forceinline__ bool test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of parity `parity` of `bar`; false after kSpin rounds.
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity)
 {
@@ -173,6 +186,17 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, in
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// tma_box with an L2 cache policy for the lines it reads
+__device__ __forceinline__ void tma_box_hint(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                             uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
 }
 

@@ -218,6 +218,61 @@ def test_partition_boundaries(G, cdt):
     assert err == 0
 
 
+@pytest.mark.parametrize("cdt", [W.F16, W.E4M3])
+def test_claim_schedules_agree_bit_for_bit(cdt):
+    """The streaming kernel hands out its work by one of two schedules: the
+    compact one (the batch ranked longest first, units where a sequence has
+    no partition left skipped, the last partitions handed out one at a time)
+    or the plain one (partition blocks x sequences x heads), taken when the
+    lengths do not rank in partition order, as with a context past
+    max_context_len.  A partition's result does not depend on which CTA took
+    it or when, so the rows both batches share come out the same, bit for
+    bit; the compact one is checked against the oracle too."""
+    rng = np.random.default_rng(31 + cdt)
+    BS, D, G, Hkv = 16, 128, 1, 2
+    P = 2 * BS
+    qdt = W.F16 if cdt == W.F16 else W.BF16
+    # 41 partitions of 32 tokens at most: claimed four partitions at a time
+    ctx = [1, 17, P - 1, P, 8 * P, 8 * P + 1, 13 * P + 5, 20 * P + 3, 31 * P, 40 * P + 7]
+    kc, vc, q, bt, ctxa = _random_problem(rng, cdt, qdt, D, BS, G, Hkv, ctx)
+    ks, vs = (0.05, 0.04) if cdt == W.E4M3 else (1.0, 1.0)
+    max_ctx = int(ctxa.max())
+    out1, err1, _ = _gpu_decode(kc, vc, cdt, q, qdt, bt, ctxa, 0.09, ks, vs, partition_size=P)
+    ref = oracle.paged_attention_decode(kc, vc, cdt, q, qdt, bt, ctxa, 0.09, ks, vs)
+    H.assert_attention_close(H.out_to_double(out1), ref, "compact schedule", qdt)
+    assert err1 == 0
+    # the same batch and one more sequence whose context is past
+    # max_context_len: it ranks first with one (zero) item, so the lengths no
+    # longer rank in partition order and the plain schedule runs
+    bt2 = np.vstack([bt, bt[:1]])
+    ctx2 = np.append(ctxa, np.int32(max_ctx + 5)).astype(np.int32)
+    q2 = np.concatenate([q, q[:1]])
+    out2, err2, _ = _gpu_decode(kc, vc, cdt, q2, qdt, bt2, ctx2, 0.09, ks, vs, partition_size=P,
+                                max_ctx=max_ctx)
+    assert err2 & B.PKV_DEVERR_CONTEXT
+    assert torch.all(out2[-1] == 0)
+    assert torch.equal(out2[:-1].view(torch.int16), out1.view(torch.int16))
+
+
+@pytest.mark.parametrize("cdt", [W.F16, W.E4M3])
+def test_schedule_with_hundreds_of_partitions(cdt):
+    """Partitions of one block over contexts of up to 600 blocks: more
+    schedule entries than the compact schedule keeps, so the plain one runs;
+    and a batch whose work is too small for a tail of full units, handed out
+    one partition at a time."""
+    rng = np.random.default_rng(37 + cdt)
+    BS, D, G, Hkv = 16, 128, 1, 2
+    qdt = W.F16 if cdt == W.F16 else W.BF16
+    ks, vs = (0.05, 0.04) if cdt == W.E4M3 else (1.0, 1.0)
+    for ctx in ([600 * BS, 5000, 33, 1], [9 * BS, 1, 2]):
+        kc, vc, q, bt, ctxa = _random_problem(rng, cdt, qdt, D, BS, G, Hkv, ctx)
+        out, err, _ = _gpu_decode(kc, vc, cdt, q, qdt, bt, ctxa, 0.09, ks, vs,
+                                  partition_size=BS)
+        ref = oracle.paged_attention_decode(kc, vc, cdt, q, qdt, bt, ctxa, 0.09, ks, vs)
+        H.assert_attention_close(H.out_to_double(out), ref, "contexts %s" % ctx, qdt)
+        assert err == 0
+
+
 @pytest.mark.parametrize("G", [1, 8])
 def test_placement_does_not_change_a_bit(G):
     """The kernels' reduction order does not depend on physical block ids."""

@@ -75,8 +75,12 @@ def test_swap_between_device_pools_and_bad_pairs():
     shape = (2, 16, 128)
     a = torch.from_numpy(rng.integers(0, 256, size=(10,) + shape, dtype=np.uint8)).cuda()
     b = torch.zeros((6,) + shape, dtype=torch.uint8, device="cuda")
-    sa = B.cache_desc(a.view(torch.float16), a.view(torch.float16).clone())
-    sb = B.cache_desc(b.view(torch.float16), b.view(torch.float16).clone())
+    # the descriptors hold raw pointers: every cache they name stays alive
+    # (a local) until the swap has finished
+    av = a.view(torch.float16).clone()
+    bv = b.view(torch.float16).clone()
+    sa = B.cache_desc(a.view(torch.float16), av)
+    sb = B.cache_desc(b.view(torch.float16), bv)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pairs = torch.tensor([[9, 5], [10, 0], [2, 6], [4, -1], [1, 1]], dtype=torch.int64,
                          device="cuda")
