@@ -138,11 +138,14 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               uint32_t tries)
 {
     const bool look = tries < tc::kSpin;
+    WaitClock clock;
     for (uint32_t i = 0; i < tries; ++i) {
         if (look ? tc::test_wait(bar, parity) : tc::try_wait(bar, parity))
             return true;
         if (*abort_flag)
             return false;
+        if (clock.expired(i))
+            break;
     }
     *abort_flag = 1;
     flag_error(dev_err, PKV_DEVERR_TIMEOUT);
@@ -679,10 +682,12 @@ __global__ void __launch_bounds__((kNC + 1) * 32, 4)
     if (threadIdx.x == 0 && *abort_flag) {
         const uint32_t armed = (uint32_t)*armed_rec;
         const uint32_t first = armed > (uint32_t)NSTG ? armed - NSTG : 0;
-        for (uint32_t tt = first; tt < armed; ++tt)
+        for (uint32_t tt = first; tt < armed; ++tt) {
+            WaitClock clock;
             for (uint32_t i = 0; i < kGroupSpin; ++i)
-                if (tc::try_wait(full0 + 8 * (tt % NSTG), (tt / NSTG) & 1))
+                if (tc::try_wait(full0 + 8 * (tt % NSTG), (tt / NSTG) & 1) || clock.expired(i))
                     break;
+        }
     }
 }
 

@@ -139,11 +139,14 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
                                              uint32_t tries)
 {
     const bool look = tries < kSpinLimit;
+    WaitClock clock;
     for (uint32_t i = 0; i < tries; ++i) {
         if (look ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))
             return true;
         if (*abort_flag)
             return false;
+        if (clock.expired(i))
+            break;
     }
     *abort_flag = 1;
     flag_error(dev_err, PKV_DEVERR_TIMEOUT);
@@ -809,16 +812,20 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
     if (threadIdx.x == 0 && *abort_flag) {
         const uint32_t armed_all = (uint32_t)drain[0];
         const uint32_t first = armed_all > (uint32_t)NSTG ? armed_all - NSTG : 0;
-        for (uint32_t tt = first; tt < armed_all; ++tt)
+        for (uint32_t tt = first; tt < armed_all; ++tt) {
+            WaitClock clock;
             for (uint32_t i = 0; i < kSpinLimit; ++i)
-                if (mbar_try_wait(&full[tt % NSTG], (tt / NSTG) & 1))
+                if (mbar_try_wait(&full[tt % NSTG], (tt / NSTG) & 1) || clock.expired(i))
                     break;
+        }
         const int pub = drain[1];
         for (int n = pub > kItemQueue ? pub - kItemQueue : 0; n < pub; ++n) {
             if (!drain[2 + n % kItemQueue])
                 continue;
+            WaitClock clock;
             for (uint32_t i = 0; i < kSpinLimit; ++i)
-                if (mbar_try_wait(&iq_full[n % kItemQueue], (n / kItemQueue) & 1))
+                if (mbar_try_wait(&iq_full[n % kItemQueue], (n / kItemQueue) & 1) ||
+                    clock.expired(i))
                     break;
         }
     }

@@ -178,6 +178,34 @@ __device__ __forceinline__ uint16_t e4m3x2_satfinite(float a, float b)
 
 // ------------------------------------------------------------------ misc
 
+// Every mbarrier wait in these kernels is bounded in polls and in time: a
+// try_wait poll may suspend the thread for a while of the hardware's choosing,
+// so a limit on polls alone does not bound how long a wait for a phase that
+// never completes takes.  A wait also gives up kWaitNs nanoseconds (by
+// %globaltimer) after its first failed poll.
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// The time bound of one wait; expired(i) after failed poll i (from 0).
+struct WaitClock {
+    uint64_t t0 = 0;
+    __device__ __forceinline__ bool expired(uint32_t i)
+    {
+        const uint64_t now = global_ns();
+        if (i == 0) {
+            t0 = now;
+            return false;
+        }
+        return now - t0 > kWaitNs;
+    }
+};
+
 __device__ __forceinline__ void flag_error(int32_t* dev_err, int32_t bit)
 {
     if (dev_err != nullptr)

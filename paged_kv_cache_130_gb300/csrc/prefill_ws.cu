@@ -102,11 +102,14 @@ __device__ __forceinline__ void set_abort(int* flag, int32_t* dev_err)
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, int* flag,
                                          int32_t* dev_err)
 {
+    WaitClock clock;
     for (uint32_t i = 0; i < kSpin; ++i) {
         if (try_wait(bar, parity))
             return true;
         if (aborted(flag))
             return false;
+        if (clock.expired(i))
+            break;
     }
     set_abort(flag, dev_err);
     return false;
@@ -117,12 +120,13 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, int* fl
                                           int32_t* dev_err)
 {
     bool ok = false;
+    WaitClock clock;
     for (uint32_t i = 0; i < kSpin; ++i) {
         if (try_wait(bar, parity)) {
             ok = true;
             break;
         }
-        if (aborted(flag))
+        if (aborted(flag) || clock.expired(i))
             break;
     }
     ok = __all_sync(0xffffffffu, ok);

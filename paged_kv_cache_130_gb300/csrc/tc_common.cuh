@@ -112,12 +112,16 @@ __device__ __forceinline__ bool test_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase of parity `parity` of `bar`; false after kSpin rounds.
+// Wait for the phase of parity `parity` of `bar`; false after kSpin polls or
+// kWaitNs nanoseconds.
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity)
 {
+    WaitClock clock;
     for (uint32_t i = 0; i < kSpin; ++i)
         if (try_wait(bar, parity))
             return true;
+        else if (clock.expired(i))
+            break;
     return false;
 }
 
