@@ -6,7 +6,8 @@ attention over every sequence (partition kernel + log-sum-exp reduce).  The
 cache is pre-filled once (untimed).  Each stage is captured once as a CUDA
 graph; the timed loop replays the graphs between CUDA events.  The decode
 inputs of every benchmark layer exceed the 129 MB L2, so no flush is needed
-(``--flush write`` adds a 512 MiB write between steps).
+(``--flush write`` adds a 512 MiB write between steps, ``--flush read`` a
+512 MiB read, which leaves L2 holding clean lines of another buffer).
 
 Output: one JSON line on rank 0.  ``value`` is decode KV-read GB/s: algorithmic
 bytes of one decode (every cached K/V element once per KV head -- a block that
@@ -48,21 +49,21 @@ FALLBACK_HBM_GBS = 6800.0
 # reported as null); "profile" names the summary under profiles/ that prints
 # the figures and the command.
 NCU_TRAFFIC = {
-    "opt13b_f16": {"bytes_per_launch": 366086912 + 3072256, "src_sha": "d3ce772ce427fdef",
+    "opt13b_f16": {"bytes_per_launch": 366120448 + 2892800, "src_sha": "c1444ed016b7e098",
                    "profile": "profiles/decode_stream_kernel_opt13b_f16.md"},
-    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642887680 + 2719232,
-                            "src_sha": "d3ce772ce427fdef",
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642895872 + 2703104,
+                            "src_sha": "c1444ed016b7e098",
                             "profile": "profiles/decode_mma_kernel_llama2_70b_bf16_gqa.md"},
-    "llama2_7b_fp8_long": {"bytes_per_launch": 2498331648 + 12674048,
-                           "src_sha": "d3ce772ce427fdef",
+    "llama2_7b_fp8_long": {"bytes_per_launch": 2497221888 + 6651904,
+                           "src_sha": "c1444ed016b7e098",
                            "profile": "profiles/decode_stream_kernel_llama2_7b_fp8_long.md"},
     # the single-pass shared-prefix kernel (the whole decode call)
     "cow_parallel_sampling_f16:shared-prefix": {
-        "bytes_per_launch": 381784832 + 2971136, "src_sha": "d3ce772ce427fdef",
+        "bytes_per_launch": 381801984 + 2453504, "src_sha": "c1444ed016b7e098",
         "profile": "profiles/decode_group_kernel_cow_parallel_sampling_f16.md"},
 }
 DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_group.cu", "decode_common.cuh",
-                  "pkv_common.cuh", "pkv_api.cu")
+                  "pkv_common.cuh", "tc_common.cuh", "pkv_api.cu")
 # the same for the prefill kernel
 NCU_PREFILL_TRAFFIC = {
     "prefill_llama2_7b_bf16": {"bytes_per_launch": 647137536 + 71322112,
@@ -154,7 +155,7 @@ def parse_args(argv=None):
                          "(GQA, copy-on-write parallel sampling, long E4M3) under a "
                          "`configs` key; none: the headline workload only; or a "
                          "comma-separated list of workload names")
-    ap.add_argument("--flush", default="none", choices=["none", "write"],
+    ap.add_argument("--flush", default="none", choices=["none", "write", "read"],
                     help="none: the decode inputs alone exceed L2; write: also write "
                          "512 MiB between steps")
     return ap.parse_args(argv)
@@ -477,7 +478,7 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
                                                 w.max_context_len, ps)
     workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
-    flush = torch.empty(FLUSH_BYTES if args.flush == "write" else 16, dtype=torch.uint8,
+    flush = torch.empty(FLUSH_BYTES if args.flush != "none" else 16, dtype=torch.uint8,
                         device=dev)
     maxp = -(-w.max_context_len // ps)
     launches_per_step = 1 + (1 if pairs is not None else 0) + 1 + (1 if maxp > 1 else 0)
@@ -507,9 +508,13 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
             B.pkv_paged_attention_partitions(desc, q, bt, cl, w.max_context_len, w.scale,
                                              partition_size=ps, workspace=workspace, out=out)
 
+    flush_sink = torch.zeros(1, dtype=torch.int64, device=dev)
+
     def maybe_flush(i):
         if args.flush == "write":
             flush.fill_(i & 0xff)
+        elif args.flush == "read":
+            flush_sink.add_(flush.view(torch.int64).sum())
 
     torch.cuda.synchronize()
     for i in range(args.warmup):
@@ -566,7 +571,7 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
     # launch streams inputs larger than L2; with --flush write a flush runs
     # between launches and is timed per launch instead)
     part_ms = []
-    if args.flush == "write":
+    if args.flush != "none":
         for i in range(args.steps):
             maybe_flush(i)
             a = torch.cuda.Event(enable_timing=True)
@@ -586,6 +591,25 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
         b.record()
         torch.cuda.synchronize()
         part_ms = [a.elapsed_time(b) / args.steps] * args.steps
+
+    # the same kernel launched alone after a 512 MiB read of another buffer
+    # (L2 then holds none of the call's lines, all clean), timed per launch:
+    # what a launch costs with nothing of it left in L2 and no overlap with
+    # a launch before it
+    cold = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    cold_sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    cold_ms = []
+    for i in range(args.steps):
+        cold_sink.add_(cold.view(torch.int64).sum())
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        replay["partitions"]()
+        b.record()
+        cold_ms.append((a, b))
+    torch.cuda.synchronize()
+    cold_ms = [a.elapsed_time(b) for a, b in cold_ms]
+    del cold
 
     # the step again as ONE graph (copy, append and decode captured
     # together, event nodes between them): the decode call's interval then
@@ -720,13 +744,15 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
                            if shared else
                            decode_kernel_name(w) + " (pkv_paged_attention_partitions)"),
                 "algorithmic_bytes": rbytes,
+                "frac_alone_after_l2_read": rbytes / (statistics.mean(cold_ms) / 1e3) / 1e9 / peak,
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
     cfg = workload_config(w)
     cfg["l2"] = ("decode inputs (%.0f MB of K/V per step) exceed the 129 MB L2; no flush"
                  % (w.kv_bytes() / 1e6) if args.flush == "none"
-                 else "512 MiB written between steps (L2 flush)")
+                 else "512 MiB %s between steps (L2 flush)"
+                 % ("written" if args.flush == "write" else "read"))
     cfg["timing"] = (("value: the decode call between event nodes inside one CUDA graph of "
                       "the whole step (copy, append, decode); separate_graphs: the same "
                       "with the step as two graphs, events between their replays; "
