@@ -66,16 +66,16 @@ DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_group.cu", "decode_co
                   "pkv_common.cuh", "tc_common.cuh", "pkv_api.cu")
 # the same for the prefill kernel
 NCU_PREFILL_TRAFFIC = {
-    "prefill_llama2_7b_bf16": {"bytes_per_launch": 647137536 + 71322112,
-                               "src_sha": "0ba540cc6e5325c3",
+    "prefill_llama2_7b_bf16": {"bytes_per_launch": 645102080 + 61541120,
+                               "src_sha": "6c93987b8c1a6914",
                                "profile": "profiles/prefill_ws_kernel_prefill_llama2_7b_bf16.md"},
     "prefill_llama2_70b_gqa_chunked_bf16": {
-        "bytes_per_launch": 183102464 + 29753600, "src_sha": "0ba540cc6e5325c3",
+        "bytes_per_launch": 177549824 + 23233280, "src_sha": "6c93987b8c1a6914",
         "profile": "profiles/prefill_ws_kernel_prefill_llama2_7b_bf16.md"},
 }
 # the same for the block-hash kernel
 NCU_HASH_TRAFFIC = {
-    "hash_prompts": {"bytes_per_launch": 21091328 + 0, "src_sha": "e776a2cab7bb853f",
+    "hash_prompts": {"bytes_per_launch": 21091328 + 0, "src_sha": "9fc632474980a784",
                      "profile": "profiles/block_hash_kernel_hash_prompts.md"},
 }
 HASH_SOURCES = ("block_hash.cu", "pkv_common.cuh")
