@@ -472,10 +472,13 @@ pkv_status pkv_paged_attention_decode_static_ws(const pkv_cache_desc* cache,
  * dev_err, stops waiting everywhere, lets the copies it started land and
  * returns, so the context stays usable.  This call sets the number of polls
  * per wait for decode calls issued afterwards (captured into their launch
- * parameters at the call): 0 restores the kernel's own limit (2^22 polls).  A
- * test sets a small value to make a wait run out on purpose and check the
- * error path.  Returns the previous setting.  Process-wide; the drain of
- * copies in flight always keeps the full limit.
+ * parameters at the call): 0 restores the kernel's own limit (2^22 polls, and
+ * at most one second from a wait's first failed poll).  Under a lower limit a
+ * poll is one look at the barrier that does not suspend the thread, so a wait
+ * that is not already complete runs out.  A test sets a small value to make a
+ * wait run out on purpose and check the error path.  Returns the previous
+ * setting.  Process-wide; the drain of copies in flight always keeps the full
+ * limit.
  * ------------------------------------------------------------------------- */
 uint32_t pkv_testing_set_decode_wait_limit(uint32_t tries);
 
