@@ -480,6 +480,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
             for (int i = 1; i < ns; ++i)
                 ok = ok && sched_n[i] <= sched_n[i - 1];
             const int maxp = sched_n[0];
+            // a table of more than kMaxSchedEntries entries is certain past
+            // this point; the scan below then is not made at all
+            ok = ok && maxp <= kMaxSchedEntries * unit_parts;
             // the first partition of the single-partition tail: the largest
             // multiple of unit_parts after which at least kTailUnits units a
             // CTA remain (0: every unit a single partition)
