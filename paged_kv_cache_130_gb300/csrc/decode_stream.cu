@@ -275,19 +275,39 @@ struct SimtTile {
         }
     }
 
-    // Totals over the warp: l over distinct tokens, acc over the lanes of one
-    // d-chunk.  Lane l < RV then holds d-chunk l.
-    __device__ __forceinline__ void finish_warp()
+    // Totals over the warp, filed into acc_out[D]: l over distinct tokens
+    // (every lane), acc over the 32 / RV lanes that hold one d-chunk.  The
+    // acc sums are a transpose reduction: each round over lane bit `off`
+    // halves the list a lane keeps (the lane with the bit set keeps the upper
+    // half), so after log2(32 / RV) rounds every lane holds D / 32 finished
+    // dims and writes them; no sum is computed twice.
+    __device__ __forceinline__ void finish_warp(int lane, float* acc_out)
     {
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1)
             l += __shfl_xor_sync(0xffffffffu, l, off);
         l *= 1.0f / DUP;                          // each token counted DUP times
+        float v[EPV];
 #pragma unroll
-        for (int off = RV; off < 32; off <<= 1)
+        for (int e = 0; e < EPV; ++e)
+            v[e] = acc(e);
+        int first = (lane % RV) * EPV;            // dim of v[0]
 #pragma unroll
-            for (int e = 0; e < EPV; ++e)
-                acc(e) += __shfl_xor_sync(0xffffffffu, acc(e), off);
+        for (int off = RV, half = EPV / 2; off < 32; off <<= 1, half >>= 1) {
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int k = 0; k < half; ++k) {
+                const float send = upper ? v[k] : v[k + half];
+                const float keep = upper ? v[k + half] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+            if (upper)
+                first += half;
+        }
+        constexpr int KEPT = D / 32;
+#pragma unroll
+        for (int k = 0; k < KEPT; ++k)
+            acc_out[first + k] = v[k];
     }
 };
 
@@ -608,16 +628,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 3)
                     if (ok && lane == 0)
                         mbar_arrive(&empty[stage]);
                 }
-                st.finish_warp();
                 // filed by block residue k0, not by warp: the merge then adds the
                 // same partial sums in the same order whichever warp held a
                 // residue (that depends on the items the CTA took before), so a
                 // result is the same from run to run, bit for bit
-                if (lane < T::RV) {
-#pragma unroll
-                    for (int e = 0; e < T::EPV; ++e)
-                        sm_acc[k0 * D + lane * T::EPV + e] = st.acc(e);
-                }
+                st.finish_warp(lane, sm_acc + k0 * D);
                 if (lane == 0) {
                     sm_m[k0] = st.m;
                     sm_l[k0] = st.l;
