@@ -49,17 +49,17 @@ FALLBACK_HBM_GBS = 6800.0
 # reported as null); "profile" names the summary under profiles/ that prints
 # the figures and the command.
 NCU_TRAFFIC = {
-    "opt13b_f16": {"bytes_per_launch": 366092032 + 2823680, "src_sha": "1daac43cee9e20f5",
+    "opt13b_f16": {"bytes_per_launch": 366086656 + 2871296, "src_sha": "a2cc1717bfee0912",
                    "profile": "profiles/decode_stream_kernel_opt13b_f16.md"},
-    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642898176 + 2702592,
-                            "src_sha": "1daac43cee9e20f5",
+    "llama2_70b_bf16_gqa": {"bytes_per_launch": 642888960 + 3087872,
+                            "src_sha": "a2cc1717bfee0912",
                             "profile": "profiles/decode_mma_kernel_llama2_70b_bf16_gqa.md"},
-    "llama2_7b_fp8_long": {"bytes_per_launch": 2497206528 + 6751488,
-                           "src_sha": "1daac43cee9e20f5",
+    "llama2_7b_fp8_long": {"bytes_per_launch": 2497219328 + 6611456,
+                           "src_sha": "a2cc1717bfee0912",
                            "profile": "profiles/decode_stream_kernel_llama2_7b_fp8_long.md"},
     # the single-pass shared-prefix kernel (the whole decode call)
     "cow_parallel_sampling_f16:shared-prefix": {
-        "bytes_per_launch": 381753344 + 3080448, "src_sha": "1daac43cee9e20f5",
+        "bytes_per_launch": 381789696 + 3032832, "src_sha": "a2cc1717bfee0912",
         "profile": "profiles/decode_group_kernel_cow_parallel_sampling_f16.md"},
 }
 DECODE_SOURCES = ("decode.cu", "decode_stream.cu", "decode_group.cu", "decode_common.cuh",
