@@ -3,8 +3,11 @@
 One step = the whole hot path over one batch: the copy-on-write block copies
 (when the workload has any), the append of the step's new tokens, and decode
 attention over every sequence (partition kernel + log-sum-exp reduce).  The
-cache is pre-filled once (untimed).  Each stage is captured once as a CUDA
-graph; the timed loop replays the graphs between CUDA events.  The decode
+cache is pre-filled once (untimed).  The step is captured as one CUDA graph
+with event nodes between its stages, and ``value`` is the decode call's
+interval inside it (``separate_graphs`` keeps the same with the step as two
+graphs, events between their replays); the roofline's kernel is launched
+back to back, and once more each launch alone after an L2 read.  The decode
 inputs of every benchmark layer exceed the 129 MB L2, so no flush is needed
 (``--flush write`` adds a 512 MiB write between steps, ``--flush read`` a
 512 MiB read, which leaves L2 holding clean lines of another buffer).
