@@ -218,8 +218,16 @@ def test_partition_boundaries(G, cdt):
     assert err == 0
 
 
+# (partition size, contexts): units of four 32-token partitions, and of two
+# 1024-token partitions
+SCHEDULE_CASES = [(32, [1, 17, 31, 32, 8 * 32, 8 * 32 + 1, 13 * 32 + 5, 20 * 32 + 3, 31 * 32,
+                        40 * 32 + 7]),
+                  (1024, [9000, 8193, 5000, 1500, 300])]
+
+
+@pytest.mark.parametrize("case", [0, 1])
 @pytest.mark.parametrize("cdt", [W.F16, W.E4M3])
-def test_claim_schedules_agree_bit_for_bit(cdt):
+def test_claim_schedules_agree_bit_for_bit(cdt, case):
     """The streaming kernel hands out its work by one of two schedules: the
     compact one (the batch ranked longest first, units where a sequence has
     no partition left skipped, the last partitions handed out one at a time)
@@ -228,12 +236,12 @@ def test_claim_schedules_agree_bit_for_bit(cdt):
     max_context_len.  A partition's result does not depend on which CTA took
     it or when, so the rows both batches share come out the same, bit for
     bit; the compact one is checked against the oracle too."""
-    rng = np.random.default_rng(31 + cdt)
+    rng = np.random.default_rng(31 + cdt + 7 * case)
     BS, D, G, Hkv = 16, 128, 1, 2
-    P = 2 * BS
+    # at least eight partitions in the longest context: claimed
+    # min(4, 2048 / P) partitions at a time
+    P, ctx = SCHEDULE_CASES[case]
     qdt = W.F16 if cdt == W.F16 else W.BF16
-    # 41 partitions of 32 tokens at most: claimed four partitions at a time
-    ctx = [1, 17, P - 1, P, 8 * P, 8 * P + 1, 13 * P + 5, 20 * P + 3, 31 * P, 40 * P + 7]
     kc, vc, q, bt, ctxa = _random_problem(rng, cdt, qdt, D, BS, G, Hkv, ctx)
     ks, vs = (0.05, 0.04) if cdt == W.E4M3 else (1.0, 1.0)
     max_ctx = int(ctxa.max())
