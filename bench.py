@@ -386,7 +386,8 @@ def workload_config(w):
             "max_context_len": w.max_context_len,
             "copy_pairs": int(len(w.copy_pairs)),
             "step_tokens": int(len(w.step_slots)),
-            "l2": "decode inputs exceed the 129 MB L2",
+            "l2": "decode inputs (%.0f MB of K/V per step) exceed the 129 MB L2; no flush"
+                  % (w.kv_bytes() / 1e6),
             "parallelism": "replicas"}
 
 
@@ -751,12 +752,14 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
+    # the workload's config, the same in the reference arm's line; how this
+    # arm measured it goes under "measurement"
     cfg = workload_config(w)
-    cfg["l2"] = ("decode inputs (%.0f MB of K/V per step) exceed the 129 MB L2; no flush"
-                 % (w.kv_bytes() / 1e6) if args.flush == "none"
-                 else "512 MiB %s between steps (L2 flush)"
-                 % ("written" if args.flush == "write" else "read"))
-    cfg["timing"] = (("value: the decode call between event nodes inside one CUDA graph of "
+    if args.flush != "none":
+        cfg["l2"] = ("512 MiB %s between steps (L2 flush)"
+                     % ("written" if args.flush == "write" else "read"))
+    measurement = {}
+    measurement["timing"] = (("value: the decode call between event nodes inside one CUDA graph of "
                       "the whole step (copy, append, decode); separate_graphs: the same "
                       "with the step as two graphs, events between their replays; "
                       if one_graph is not None else
@@ -764,16 +767,16 @@ def run_gpu(args, w, cpu_budget_s=15.0, sample_cap_bytes=None, threads=8):
                      + "roofline: the partition kernel launched `steps` times back to back "
                      "between one pair of events; e2e: see e2e.timing") \
         if not args.no_graphs else "CUDA events around direct calls"
-    cfg["partition_size"] = ps
-    cfg["shared_prefix"] = ({"groups": int(len(grp_blocks)), "max_group": max_group,
-                             "prefix_blocks": max_prefix,
-                             "route": "single pass" if single else "split"}
-                            if shared else None)
+    measurement["partition_size"] = ps
+    measurement["shared_prefix"] = ({"groups": int(len(grp_blocks)), "max_group": max_group,
+                                     "prefix_blocks": max_prefix,
+                                     "route": "single pass" if single else "split"}
+                                    if shared else None)
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": cfg,
+            "config": cfg, "measurement": measurement,
             "hbm_frac": value / peak,
             "decode_ms": dec_s * 1e3 / args.steps,
             "decode_tokens_per_s": w.num_seqs * world * args.steps / dec_s,
@@ -823,7 +826,7 @@ def config_summary(line):
     keep = ("value", "unit", "hbm_frac", "decode_ms", "ms_per_step", "decode_tokens_per_s",
             "model_tokens_per_s_attention_only", "decode_ms_spread", "decode_bytes",
             "unique_kv_bytes", "logical_bytes_gbs", "roofline", "e2e", "gpu_launches", "clocks",
-            "cpu_baseline", "config")
+            "cpu_baseline", "config", "measurement")
     return {k: line[k] for k in keep if k in line}
 
 
