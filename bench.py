@@ -903,8 +903,8 @@ def prefill_config(w):
     cfg = workload_config(w)
     cfg.update({"new_tokens": w.total_q, "max_q_len": w.max_q_len,
                 "cached_tokens": int(w.context_lens.sum()) - w.total_q,
-                "l2": "K/V of the batch (%.0f MB) are read once per 64-row query tile; "
-                      "compute-bound, no flush" % (w.kv_bytes() / 1e6)})
+                "l2": "K/V of the batch (%.0f MB) are read once per CTA (two 128-row "
+                      "query tiles); compute-bound, no flush" % (w.kv_bytes() / 1e6)})
     return cfg
 
 
